@@ -1,0 +1,156 @@
+"""fp64 CPU oracle for sparse latent attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never loads it and
+shares no code with it.
+
+The arithmetic lives in ``sa_oracle.c`` (plain C, fp64, OpenMP over queries);
+this module compiles it with gcc on first use and exposes numpy-facing
+wrappers:
+
+* :func:`sparse_attn`   -- the ``sparse_attn(q, kv, attn_sink, topk_idxs,
+  softmax_scale)`` step of the "DeepSeek-V4.1 > Output projection" page
+  (``Attention.forward`` excerpt), with the sink as an extra softmax logit and
+  -1 as "skip";
+* :func:`inverse_rope`  -- ``apply_rotary_emb(o[..., -rd:], freqs_cis, True)``
+  read as consecutive complex pairs rotated by ``-pos * theta**(-2i/rd)``;
+* :func:`wo_a`          -- the block-diagonal ``einsum("bsgd,grd->bsgr")``.
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against a dense
+masked brute force, closed forms and invariants; nothing here is "parity
+unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``sa_oracle.c`` into ``libsa_oracle.so`` next to it."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.sa_oracle_sparse_attn.restype = i64
+            lib.sa_oracle_sparse_attn.argtypes = [P, P, P, P, f64, i32, i32, i32,
+                                                  i32, i32, i32, P, i64, P, i32]
+            lib.sa_oracle_inverse_rope.restype = None
+            lib.sa_oracle_inverse_rope.argtypes = [P, i64, P, i32, i32, i32, f64, i32]
+            lib.sa_oracle_wo_a.restype = None
+            lib.sa_oracle_wo_a.argtypes = [P, P, i64, i32, i32, i32, P, i32]
+            lib.sa_oracle_threads.restype = i32
+            lib.sa_oracle_threads.argtypes = [i32]
+            _lib = lib
+    return _lib
+
+
+def threads(n: int = 0) -> int:
+    """How many OpenMP threads a call with ``n_threads=n`` uses (0 = all)."""
+    return int(_load().sa_oracle_threads(int(n)))
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _as_bf16_bits(x) -> np.ndarray:
+    """Accept raw bf16 bits (uint16/int16 numpy) or a torch bf16 tensor."""
+    if hasattr(x, "view") and hasattr(x, "dtype") and str(x.dtype) == "torch.bfloat16":
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype not in (np.uint16, np.int16):
+        raise TypeError("expected bf16 bit patterns (uint16) or a torch.bfloat16 tensor")
+    return a.view(np.uint16)
+
+
+def _np(x, dtype) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(x, dtype=dtype)
+
+
+def sparse_attn(q, kv, sink, idx, scale: float, queries=None, n_threads: int = 0):
+    """fp64 ``sparse_attn``.
+
+    q bf16 [B,T,H,D]; kv bf16 [B,N,D]; sink fp32 [H]; idx int32 [B,T,K].
+    ``queries``: optional 1-D list of flattened query numbers ``b*T+t``.
+    Returns (out fp64 [n_queries,H,D] -- [B,T,H,D] when ``queries`` is None,
+    number of queries that met an index outside [-1, N)).
+    """
+    qb, kvb = _as_bf16_bits(q), _as_bf16_bits(kv)
+    B, T, H, D = qb.shape
+    Bk, N, Dk = kvb.shape
+    s = _np(sink, np.float32)
+    ix = _np(idx, np.int32)
+    if Bk != B or Dk != D or s.shape != (H,) or ix.shape[:2] != (B, T):
+        raise ValueError("shape mismatch")
+    K = ix.shape[2]
+    if queries is None:
+        ql, nq, qp = None, B * T, None
+    else:
+        ql = np.ascontiguousarray(queries, dtype=np.int64).reshape(-1)
+        if ql.size and (ql.min() < 0 or ql.max() >= B * T):
+            raise ValueError("query number out of range")
+        nq, qp = ql.size, _ptr(ql)
+    out = np.zeros((nq, H, D), dtype=np.float64)
+    bad = _load().sa_oracle_sparse_attn(_ptr(qb), _ptr(kvb), _ptr(s), _ptr(ix),
+                                        float(scale), B, T, H, D, N, K, qp, nq,
+                                        _ptr(out), int(n_threads))
+    if queries is None:
+        out = out.reshape(B, T, H, D)
+    return out, int(bad)
+
+
+def inverse_rope(o: np.ndarray, pos, rope_dim: int, theta: float, n_threads: int = 0):
+    """In-place-free inverse rotary embedding of the last ``rope_dim`` features.
+
+    o fp64 [..., H, D]; pos int [...] (one position per row of o).
+    """
+    x = np.array(o, dtype=np.float64, copy=True, order="C")
+    H, D = x.shape[-2:]
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.int64),
+                                             x.shape[:-2])).reshape(-1)
+    n = p.size
+    _load().sa_oracle_inverse_rope(_ptr(x), n, _ptr(p), H, D, int(rope_dim),
+                                   float(theta), int(n_threads))
+    return x
+
+
+def wo_a(o: np.ndarray, W, n_threads: int = 0):
+    """Grouped projection: o fp64 [n, G, Din], W bf16 [G, R, Din] -> fp64 [n, G, R]."""
+    x = np.ascontiguousarray(o, dtype=np.float64)
+    w = _as_bf16_bits(W)
+    G, R, Din = w.shape
+    lead = x.shape[:-2]
+    if x.shape[-2:] != (G, Din):
+        raise ValueError("o must end in [G, Din]")
+    n = int(np.prod(lead)) if lead else 1
+    y = np.zeros(lead + (G, R), dtype=np.float64)
+    _load().sa_oracle_wo_a(_ptr(x), _ptr(w), n, G, R, Din, _ptr(y), int(n_threads))
+    return y

@@ -1,0 +1,298 @@
+"""Pins for the fp64 oracle, checked against things other than itself.
+
+* a dense masked-attention brute force in the pattern of the "GLM-5 > Sparse
+  latent attention" page (``eager_attention_forward`` plus the index mask built
+  with ``scatter`` and filled with -inf), with the sink appended as one more
+  logit whose value row is zero;
+* a pure-Python scalar brute force on a very small case;
+* closed forms: one valid index, equal scores, sink -> -inf, a dominant sink;
+* invariants: permutation of the index list, -1 anywhere, the all-skip row,
+  K = 0, repeated indices counted as separate terms, a one-hot index probe;
+* the rotary embedding's special angles, group law and complex-number form;
+* the grouped projection against a dense block-diagonal matmul.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+RNG = np.random.default_rng(1234)
+
+
+def bf16(x):
+    return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def f64(t):
+    return t.to(torch.float32).numpy().astype(np.float64)
+
+
+def rand_case(B, T, H, D, N, K, p_skip=0.3, seed=0, distinct=True):
+    rng = np.random.default_rng(seed)
+    q = bf16(rng.standard_normal((B, T, H, D)))
+    kv = bf16(rng.standard_normal((B, N, D)))
+    sink = rng.standard_normal(H).astype(np.float32)
+    idx = np.empty((B, T, K), dtype=np.int32)
+    for b in range(B):
+        for t in range(T):
+            if distinct:
+                row = rng.permutation(N)[:K]
+            else:
+                row = rng.integers(0, N, size=K)
+            row = np.where(rng.random(K) < p_skip, -1, row)
+            idx[b, t] = row
+    return q, kv, sink, idx
+
+
+def dense_bruteforce(q, kv, sink, idx, scale):
+    """Dense masked softmax attention: every latent row scored, the rows not in
+    the list masked with -inf, the sink appended as an extra logit (zero value)."""
+    qd, kvd = f64(q), f64(kv)
+    B, T, H, D = qd.shape
+    N = kvd.shape[1]
+    out = np.zeros((B, T, H, D))
+    for b in range(B):
+        for t in range(T):
+            keep = np.zeros(N, dtype=bool)
+            sel = idx[b, t][idx[b, t] >= 0]
+            keep[sel] = True
+            logits = (qd[b, t] @ kvd[b].T) * scale                  # [H, N]
+            logits = np.where(keep[None, :], logits, -np.inf)
+            logits = np.concatenate([logits, sink.astype(np.float64)[:, None]], 1)
+            m = logits.max(1, keepdims=True)
+            e = np.exp(logits - m)
+            p = e / e.sum(1, keepdims=True)
+            vals = np.concatenate([kvd[b], np.zeros((1, D))], 0)    # sink row carries no value
+            out[b, t] = p @ vals
+    return out
+
+
+@pytest.mark.parametrize("H,D,N,K", [(1, 8, 24, 10), (4, 16, 40, 17), (64, 512, 64, 48)])
+def test_dense_bruteforce(H, D, N, K):
+    q, kv, sink, idx = rand_case(2, 3, H, D, N, K, seed=H + D)
+    scale = D ** -0.5
+    ref = dense_bruteforce(q, kv, sink, idx, scale)
+    got, bad = oracle.sparse_attn(q, kv, sink, idx, scale)
+    assert bad == 0
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_scalar_python_bruteforce():
+    q, kv, sink, idx = rand_case(1, 2, 2, 4, 7, 5, seed=7)
+    qd, kvd = f64(q), f64(kv)
+    scale = 0.37
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, scale)
+    for t in range(2):
+        for h in range(2):
+            terms = []
+            for j in idx[0, t]:
+                if j < 0:
+                    continue
+                s = scale * sum(float(qd[0, t, h, d]) * float(kvd[0, j, d]) for d in range(4))
+                terms.append((s, [float(kvd[0, j, d]) for d in range(4)]))
+            logits = [s for s, _ in terms] + [float(sink[h])]
+            m = max(logits)
+            den = sum(math.exp(x - m) for x in logits)
+            o = [sum(math.exp(s - m) * r[d] for s, r in terms) / den for d in range(4)]
+            np.testing.assert_allclose(got[0, t, h], o, rtol=1e-13, atol=1e-15)
+
+
+def test_single_valid_index_closed_form():
+    q, kv, sink, idx = rand_case(1, 1, 8, 32, 12, 6, seed=3)
+    idx[:] = -1
+    idx[0, 0, 4] = 9
+    scale = 32 ** -0.5
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, scale)
+    row = f64(kv)[0, 9]
+    s = scale * (f64(q)[0, 0] @ row)                        # [H]
+    w = np.exp(s) / (np.exp(s) + np.exp(sink.astype(np.float64)))
+    np.testing.assert_allclose(got[0, 0], w[:, None] * row[None, :], rtol=1e-13)
+
+
+def test_dominant_sink():
+    """sink = +8 with large logits: the sink share is visible, not ~0.1%."""
+    q, kv, sink, idx = rand_case(1, 1, 4, 16, 8, 4, seed=5)
+    q = bf16(4.0 * f64(q))
+    sink = np.full(4, 8.0, dtype=np.float32)
+    idx[:] = -1
+    idx[0, 0, 0] = 3
+    scale = 16 ** -0.5
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, scale)
+    row = f64(kv)[0, 3]
+    s = scale * (f64(q)[0, 0] @ row)
+    w = 1.0 / (1.0 + np.exp(8.0 - s))
+    np.testing.assert_allclose(got[0, 0], w[:, None] * row[None, :], rtol=1e-12)
+    assert np.all(w < 0.99)
+
+
+def test_sink_minus_inf_is_plain_softmax():
+    q, kv, sink, idx = rand_case(2, 2, 4, 16, 20, 9, seed=11)
+    sink = np.full(4, -np.inf, dtype=np.float32)
+    scale = 0.25
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, scale)
+    qd, kvd = f64(q), f64(kv)
+    for b in range(2):
+        for t in range(2):
+            sel = idx[b, t][idx[b, t] >= 0]
+            s = scale * qd[b, t] @ kvd[b, sel].T
+            p = np.exp(s - s.max(1, keepdims=True))
+            p /= p.sum(1, keepdims=True)
+            np.testing.assert_allclose(got[b, t], p @ kvd[b, sel], rtol=1e-12, atol=1e-15)
+    # a single index with sink -inf returns the row exactly
+    idx[:] = -1
+    idx[0, 0, 2] = 5
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, scale)
+    assert np.array_equal(got[0, 0], np.broadcast_to(kvd[0, 5], (4, 16)))
+
+
+def test_equal_scores_mean():
+    """q = 0: every score is 0, o = mean(rows) * n / (n + e^sink)."""
+    _, kv, sink, idx = rand_case(1, 1, 3, 8, 30, 12, seed=13)
+    q = bf16(np.zeros((1, 1, 3, 8)))
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, 0.5)
+    sel = idx[0, 0][idx[0, 0] >= 0]
+    n = sel.size
+    mean = f64(kv)[0, sel].mean(0)
+    factor = n / (n + np.exp(sink.astype(np.float64)))
+    np.testing.assert_allclose(got[0, 0], factor[:, None] * mean[None, :], rtol=1e-13)
+
+
+def test_permutation_invariance_and_skip_anywhere():
+    q, kv, sink, idx = rand_case(2, 4, 8, 64, 50, 30, p_skip=0.4, seed=17)
+    scale = 64 ** -0.5
+    ref, _ = oracle.sparse_attn(q, kv, sink, idx, scale)
+    rng = np.random.default_rng(0)
+    perm = idx.copy()
+    for b in range(2):
+        for t in range(4):
+            perm[b, t] = perm[b, t][rng.permutation(30)]
+    got, _ = oracle.sparse_attn(q, kv, sink, perm, scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-15)
+    # padding the list with -1 (front or back) changes nothing
+    pad = np.full((2, 4, 7), -1, dtype=np.int32)
+    got2, _ = oracle.sparse_attn(q, kv, sink, np.concatenate([pad, idx, pad], 2), scale)
+    np.testing.assert_allclose(got2, ref, rtol=1e-12, atol=1e-15)
+
+
+def test_all_skip_and_empty_lists_give_zero():
+    q, kv, sink, idx = rand_case(1, 3, 4, 16, 10, 5, seed=19)
+    idx[:] = -1
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, 0.3)
+    assert np.array_equal(got, np.zeros_like(got))
+    got, _ = oracle.sparse_attn(q, kv, np.full(4, -np.inf, np.float32), idx, 0.3)
+    assert np.array_equal(got, np.zeros_like(got))
+    got, _ = oracle.sparse_attn(q, kv, sink, np.zeros((1, 3, 0), np.int32), 0.3)
+    assert got.shape == (1, 3, 4, 16) and not got.any()
+
+
+def test_repeated_index_counts_twice():
+    _, kv, _, _ = rand_case(1, 1, 2, 8, 6, 3, seed=23)
+    q = bf16(np.zeros((1, 1, 2, 8)))
+    sink = np.full(2, -np.inf, dtype=np.float32)
+    idx = np.array([[[4, 1, 4]]], dtype=np.int32)
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, 1.0)
+    kvd = f64(kv)[0]
+    np.testing.assert_allclose(got[0, 0], np.broadcast_to((2 * kvd[4] + kvd[1]) / 3, (2, 8)),
+                               rtol=1e-15)
+
+
+def test_index_probe_multiplicities():
+    """q = 0, sink = -inf, row r of kv = e_r: o * V equals each row's multiplicity."""
+    N, D, K = 40, 64, 50
+    kv = bf16(np.eye(N, D)[None])
+    q = bf16(np.zeros((1, 2, 3, D)))
+    sink = np.full(3, -np.inf, dtype=np.float32)
+    rng = np.random.default_rng(29)
+    idx = rng.integers(-1, N, size=(1, 2, K)).astype(np.int32)
+    got, _ = oracle.sparse_attn(q, kv, sink, idx, 1.0)
+    for t in range(2):
+        valid = idx[0, t][idx[0, t] >= 0]
+        counts = np.bincount(valid, minlength=D)
+        np.testing.assert_allclose(got[0, t] * valid.size, np.broadcast_to(counts, (3, D)),
+                                   atol=1e-12)
+
+
+def test_out_of_range_index_is_reported_and_skipped():
+    q, kv, sink, idx = rand_case(1, 2, 2, 8, 10, 4, p_skip=0.0, seed=31)
+    clean, bad0 = oracle.sparse_attn(q, kv, sink, idx, 0.5)
+    assert bad0 == 0
+    idx2 = np.concatenate([idx, np.array([[[10], [-2]]], dtype=np.int32)], 2)
+    got, bad = oracle.sparse_attn(q, kv, sink, idx2, 0.5)
+    assert bad == 2
+    np.testing.assert_allclose(got, clean, rtol=1e-14)
+
+
+def test_query_subset_matches_full():
+    q, kv, sink, idx = rand_case(2, 5, 4, 16, 30, 12, seed=37)
+    full, _ = oracle.sparse_attn(q, kv, sink, idx, 0.25)
+    sub, _ = oracle.sparse_attn(q, kv, sink, idx, 0.25, queries=[7, 0, 4])
+    flat = full.reshape(10, 4, 16)
+    assert np.array_equal(sub, flat[[7, 0, 4]])
+
+
+# ---------------------------------------------------------------- rotary
+
+
+def test_rope_position_zero_is_identity_and_prefix_untouched():
+    x = RNG.standard_normal((3, 4, 128))
+    y = oracle.inverse_rope(x, np.zeros(3, np.int64), 64, 160000.0)
+    assert np.array_equal(y, x)
+    y = oracle.inverse_rope(x, np.array([5, 77, 4095]), 64, 160000.0)
+    assert np.array_equal(y[..., :64], x[..., :64])
+
+
+def test_rope_special_angles():
+    x = np.zeros((1, 1, 64))
+    x[0, 0, 0] = 1.0            # pair 0 = (1, 0); frequency theta**0 = 1
+    x[0, 0, 33] = 1.0           # pair 16 = (0, 1); frequency 160000**-0.5 = 1/400
+    y = oracle.inverse_rope(x, np.array([1]), 64, 160000.0)
+    np.testing.assert_allclose(y[0, 0, :2], [math.cos(1.0), -math.sin(1.0)], rtol=1e-15)
+    y = oracle.inverse_rope(x, np.array([400]), 64, 160000.0)
+    np.testing.assert_allclose(y[0, 0, 32:34], [math.sin(1.0), math.cos(1.0)], rtol=1e-12)
+
+
+def test_rope_norm_group_law_and_complex_form():
+    x = RNG.standard_normal((5, 2, 96))
+    p1 = np.array([3, 10, 100, 1000, 4095])
+    p2 = np.array([7, 1, 50, 3, 1])
+    y = oracle.inverse_rope(x, p1, 64, 160000.0)
+    pairs = lambda a: a[..., 32:].reshape(5, 2, 32, 2)
+    np.testing.assert_allclose(np.linalg.norm(pairs(y), axis=-1),
+                               np.linalg.norm(pairs(x), axis=-1), rtol=1e-13)
+    yy = oracle.inverse_rope(y, p2, 64, 160000.0)
+    np.testing.assert_allclose(yy, oracle.inverse_rope(x, p1 + p2, 64, 160000.0),
+                               rtol=1e-9, atol=1e-12)
+    # the forward embedding as complex multiplication by exp(+i p w), then the inverse
+    w = 160000.0 ** (-np.arange(32) * 2.0 / 64)
+    z = pairs(x)[..., 0] + 1j * pairs(x)[..., 1]
+    zf = z * np.exp(1j * p1[:, None, None] * w[None, None, :])
+    xf = x.copy()
+    xf[..., 32:] = np.stack([zf.real, zf.imag], -1).reshape(5, 2, 64)
+    np.testing.assert_allclose(oracle.inverse_rope(xf, p1, 64, 160000.0), x,
+                               rtol=1e-9, atol=1e-12)
+
+
+# ---------------------------------------------------------------- wo_a
+
+
+def test_wo_a_single_group_is_matmul():
+    o = RNG.standard_normal((6, 1, 40))
+    W = bf16(RNG.standard_normal((1, 24, 40)))
+    y = oracle.wo_a(o, W)
+    np.testing.assert_allclose(y[:, 0], o[:, 0] @ f64(W)[0].T, rtol=1e-12)
+
+
+def test_wo_a_block_diagonal_dense():
+    G, R, Din, n = 4, 12, 20, 9
+    o = RNG.standard_normal((n, G, Din))
+    W = bf16(RNG.standard_normal((G, R, Din)))
+    Wd = f64(W)
+    full = np.zeros((G * R, G * Din))
+    for g in range(G):
+        full[g * R:(g + 1) * R, g * Din:(g + 1) * Din] = Wd[g]
+    y = oracle.wo_a(o, W)
+    np.testing.assert_allclose(y.reshape(n, G * R), o.reshape(n, G * Din) @ full.T,
+                               rtol=1e-12, atol=1e-13)
