@@ -1,0 +1,406 @@
+"""Benchmark of the sparse latent attention path on one GB300.
+
+Default (our arm): the decode workload (B=64 queries, 640-entry index lists,
+8192-token context at ratio 2 -> 4224 latent rows per batch row), timed as one
+`sa_sparse_attn` call per step over rotating input sets whose total size
+exceeds L2, replayed from a CUDA graph.  Prints ONE JSON line.  The prefill,
+long-context decode and fused-tail workloads are measured too and reported
+under "workloads".
+
+--impl reference: the fp64 CPU oracle, timed as it stands on the host cores
+on a bounded sample of the same workload (the only reference this path has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_latent_attention_02_gb300 import inputs as I  # noqa: E402
+
+METRIC = "sparse_attn queries/s; decode gathered-KV GB/s & prefill TFLOP/s vs GB300 roofline"
+HEADLINE = "decode"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def algorithmic(wl: I.Workload, idx: torch.Tensor) -> dict:
+    """Bytes and flops the method must move / do for one call on these lists.
+
+    bytes: every valid gathered row (D bf16), q, the output, the index lists
+    and the sink; flops: 4 * H * D per valid (query, row) pair (QK^T and PV).
+    """
+    pairs = int((idx >= 0).sum().item())
+    out_bytes = 4 if wl.out_f32 else 2
+    nbytes = (pairs * wl.D * 2 + wl.n_queries * wl.H * wl.D * (2 + out_bytes)
+              + idx.numel() * 4 + wl.H * 4)
+    flops = 4 * wl.H * wl.D * pairs
+    if wl.tail:
+        din = wl.H * wl.D // wl.G
+        flops += 2 * wl.n_queries * wl.G * wl.R * din
+        nbytes += wl.G * wl.R * din * 2 + wl.n_queries * wl.G * wl.R * 2 - wl.n_queries * wl.H * wl.D * 2
+    return {"pairs": pairs, "bytes": nbytes, "flops": flops}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = None
+        if not inside:
+            # the timed region was shorter than the sampling interval: use the
+            # samples nearest to it
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for (_, p) in near]
+            note = "timed region shorter than the 100 ms sampling interval; nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[4 + i].lower().startswith("active")})
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def l2_bytes() -> int:
+    try:
+        return int(torch.cuda.get_device_properties(0).L2_cache_size)
+    except Exception:
+        return 129 * 2 ** 20
+
+
+def make_sets(wl: I.Workload, n_sets: int, seed: int, dev) -> list:
+    return [I.make_inputs(wl, seed=seed + 17 * i, device=dev) for i in range(n_sets)]
+
+
+def sets_for(wl: I.Workload, dev, seed=0, min_sets=2) -> list:
+    """Enough independent input sets that one rotation touches > 2x L2."""
+    probe = I.make_inputs(wl, seed=seed, device=dev)
+    a = algorithmic(wl, probe["idx"])
+    n = max(min_sets, int(np.ceil(2.5 * l2_bytes() / max(a["bytes"], 1))))
+    n = min(n, 8)
+    return [probe] + make_sets(wl, n - 1, seed + 1, dev)
+
+
+def time_graph_steps(step_fns, steps: int, warmup: int):
+    """Capture `steps` calls (rotating over step_fns) into one CUDA graph, warm
+    up with a `warmup`-step graph, then time one replay with CUDA events on
+    the capturing stream.  Returns seconds for the `steps` calls."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for f in step_fns:          # one eager pass (library attributes, allocations)
+            f()
+    torch.cuda.synchronize()
+    gw = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gw, stream=s):
+        for i in range(warmup):
+            step_fns[i % len(step_fns)]()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(steps):
+            step_fns[i % len(step_fns)]()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        gw.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+        e1.synchronize()
+        t1 = time.time()
+    return e0.elapsed_time(e1) / 1e3, (t0, t1)
+
+
+# ------------------------------------------------------------------ our arm
+
+def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, sampler=None):
+    import sparse_latent_attention_02_gb300 as sa
+    wl = I.WORKLOADS[name]
+    sets = sets_for(wl, dev)
+    outs = []
+    fns = []
+    if wl.tail:
+        rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).to(dev)
+        for x in sets:
+            y = torch.empty((wl.B, wl.T, wl.G * wl.R), dtype=torch.bfloat16, device=dev)
+            ws = torch.zeros(sa.fused_workspace_size(wl.B, wl.T, wl.K, wl.G, wl.R),
+                             dtype=torch.uint8, device=dev)
+            outs.append((y, ws))
+            fns.append(lambda x=x, y=y, ws=ws: sa.sparse_attn_rope_wo_a(
+                x["q"], x["kv"], x["sink"], x["idx"], wl.scale, rope, x["wo_a"], out=y,
+                workspace=ws))
+    else:
+        odt = torch.float32 if wl.out_f32 else torch.bfloat16
+        for x in sets:
+            o = torch.empty((wl.B, wl.T, wl.H, wl.D), dtype=odt, device=dev)
+            ws = torch.zeros(sa.workspace_size(wl.B, wl.T, wl.K), dtype=torch.uint8, device=dev)
+            outs.append((o, ws))
+            fns.append(lambda x=x, o=o, ws=ws: sa.sparse_attn(
+                x["q"], x["kv"], x["sink"], x["idx"], wl.scale, out=o, workspace=ws))
+    secs, (t0, t1) = time_graph_steps(fns, steps, warmup)
+    for _, ws in outs:
+        sa.check_errors(ws)
+    work = [algorithmic(wl, x["idx"]) for x in sets]
+    per_step_bytes = np.mean([w["bytes"] for w in work])
+    per_step_flops = np.mean([w["flops"] for w in work])
+    step_s = secs / steps
+    res = {
+        "workload": name, "B": wl.B, "T": wl.T, "K": wl.K, "N": wl.N,
+        "input_sets": len(sets), "steps": steps, "ms_per_step": step_s * 1e3,
+        "queries_per_s": wl.n_queries / step_s,
+        "gbs": per_step_bytes / step_s / 1e9, "tflops": per_step_flops / step_s / 1e12,
+        "bytes_per_step": int(per_step_bytes), "flops_per_step": int(per_step_flops),
+        "valid_pairs_per_step": int(np.mean([w["pairs"] for w in work])),
+        "window": (t0, t1),
+    }
+    if with_e2e:
+        res["e2e"] = bench_e2e(wl, sets[0], steps, warmup, dev)
+    del sets, outs, fns
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_e2e(wl: I.Workload, x: dict, steps: int, warmup: int, dev) -> dict:
+    """Same call end to end: every step copies all of its inputs from pinned
+    host memory, runs the C-ABI call and copies the output back."""
+    import sparse_latent_attention_02_gb300 as sa
+    keys = ["q", "kv", "sink", "idx"]
+    host = {k: x[k].cpu().pin_memory() for k in keys}
+    devb = {k: torch.empty_like(x[k]) for k in keys}
+    out = torch.empty((wl.B, wl.T, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ws = torch.zeros(sa.workspace_size(wl.B, wl.T, wl.K), dtype=torch.uint8, device=dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = out.numel() * out.element_size()
+
+    def step():
+        for k in keys:
+            devb[k].copy_(host[k], non_blocking=True)
+        sa.sparse_attn(devb["q"], devb["kv"], devb["sink"], devb["idx"], wl.scale, out=out,
+                       workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    sa.check_errors(ws)
+    secs = e0.elapsed_time(e1) / 1e3
+    return {"value": wl.n_queries * steps / secs, "unit": "queries/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
+    """The fp64 oracle, as it stands, on the host cores: whole decode steps
+    (all queries of one input set) repeated until about `budget_s` seconds."""
+    import oracle
+    wl = I.WORKLOADS[name]
+    x = I.make_inputs(wl, seed=0)
+    cores = oracle.threads(0)
+    oracle.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)   # warm
+    done, t0 = 0, time.time()
+    while True:
+        oracle.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
+        done += 1
+        if time.time() - t0 >= budget_s or done >= 1000:
+            break
+    secs = time.time() - t0
+    return {"value": wl.n_queries * done / secs, "unit": "queries/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{done} full {name} steps ({wl.n_queries} queries each), fp64, "
+                      f"{secs:.1f} s on {cores} host threads"}
+
+
+def run_ours(args):
+    import sparse_latent_attention_02_gb300 as sa
+    sa.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    head = bench_workload(HEADLINE, args.steps, args.warmup, dev, with_e2e=True)
+    clocks = sampler.summary(*head.pop("window"))
+    extra = {}
+    if not args.headline_only:
+        for name in ("long_decode", "prefill", "fused_tail"):
+            steps = max(3, min(args.steps, 20))
+            r = bench_workload(name, steps, max(args.warmup, 3), dev, with_e2e=False)
+            r["clocks"] = sampler.summary(*r.pop("window"))
+            if name in ("prefill", "fused_tail"):
+                r["roofline"] = {"bound": "tensor", "achieved": r["tflops"],
+                                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                                 "frac": r["tflops"] / pk["bf16_tflops_sustained"],
+                                 "peak_note": f"{pk['source']} sustained bf16"}
+            else:
+                r["roofline"] = {"bound": "hbm", "achieved": r["gbs"], "peak": pk["hbm_gbs"],
+                                 "unit": "GB/s", "frac": r["gbs"] / pk["hbm_gbs"],
+                                 "peak_note": f"{pk['source']} HBM copy"}
+            extra[name] = r
+    sampler.stop()
+    e2e = head.pop("e2e")
+    cpu = cpu_baseline(HEADLINE, budget_s=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": head["queries_per_s"], "unit": "queries/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{HEADLINE}: B={head['B']} T={head['T']} H=64 D=512 "
+                               f"N={head['N']} K={head['K']}",
+                   "parallelism": "replicas only (one GPU)",
+                   "l2": f"inputs rotate over {head['input_sets']} independent sets "
+                         f"(> 2x L2 per rotation)",
+                   "timing": "CUDA graph of `steps` calls, CUDA events on its stream"},
+        "gbs": head["gbs"], "tflops": head["tflops"],
+        "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": head["gbs"] / pk["hbm_gbs"],
+                     "traffic": None,
+                     "note": f"peak = {pk['source']} HBM copy; achieved = algorithmic bytes "
+                             f"({head['bytes_per_step']} per call) / call duration"},
+        "e2e": e2e,
+        "gpu_launches": None,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "workloads": extra,
+    }
+    print(json.dumps(line))
+
+
+def run_reference(args):
+    import oracle
+    wl = I.WORKLOADS[HEADLINE]
+    x = I.make_inputs(wl, seed=0)
+    cores = oracle.threads(0)
+    # each step: a bounded sample (a quarter of the decode batch) of the workload
+    sample = np.arange(0, wl.n_queries, 4, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, queries=sample)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, queries=sample)
+    secs = time.time() - t0
+    v = sample.size * args.steps / secs
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "queries/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{HEADLINE}: B={wl.B} T={wl.T} H=64 D=512 N={wl.N} K={wl.K}"},
+        "cpu_baseline": {"value": v, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample.size} of {wl.n_queries} decode queries per step"},
+        "e2e": {"value": v, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    if world > 1:
+        # replicas only: each rank runs its own GPU; rank 0 reports
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if rank == 0:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,139 @@
+/*
+ * sa.h -- C ABI of the GB300 (sm_103a) sparse latent attention library.
+ *
+ * The operation is the `sparse_attn(q, kv, attn_sink, topk_idxs,
+ * softmax_scale)` step of DeepSeek-V4.1's attention, as called in the
+ * `Attention.forward` excerpt of the "DeepSeek-V4.1 > Output projection" page,
+ * together with the two steps that follow it there: the inverse rotary
+ * embedding of the last rope_head_dim output features and the block-diagonal
+ * grouped projection `einsum("bsgd,grd->bsgr", o, wo_a)`.
+ *
+ * For every query (b, t) and head h, with S the list entries idx[b,t,j] != -1:
+ *   s_j    = scale * <q[b,t,h,:], kv[b, idx_j, :]>
+ *   M      = max(sink[h], max_j s_j)
+ *   o[h,:] = sum_j e^(s_j - M) kv[b, idx_j, :] / (e^(sink[h] - M) + sum_j e^(s_j - M))
+ * All heads share the gathered latent rows, which serve as both keys and
+ * values.  The sink is one extra logit per head with no value row and is not
+ * multiplied by the scale.  An entry of -1 contributes nothing wherever it
+ * sits in the list; any other listed entry contributes one term (a repeated
+ * index counts twice).  An empty list gives o = 0.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers name memory on the current CUDA device; the caller owns
+ *     all of it.  The library keeps no per-call state and allocates nothing.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
+ *     is enqueued asynchronously on it; host-detectable argument errors return
+ *     before anything is enqueued.
+ *   - Device-detected problems (an index outside [-1, N), a bounded internal
+ *     wait that ran out) are OR-ed into an error word at the start of the
+ *     workspace; `sa_check_errors` synchronises the stream, reads and clears
+ *     it.  The kernels never trap: a bad index is skipped.
+ *   - The workspace must be zero-filled before its first use (the error word
+ *     and internal counters start at zero); the library leaves it reusable.
+ *     Two calls that share a workspace must not run concurrently.
+ *   - Fast path only: H == 64 heads, D == 512 features; other shapes return
+ *     SA_ERR_UNSUPPORTED.  1 <= K <= SA_MAX_K, or K == 0 (all-zero output).
+ */
+#ifndef SA_H_
+#define SA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SA_OK = 0,
+    SA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer */
+    SA_ERR_UNSUPPORTED = 2,   /* shape outside the fast path (H, D, K, rope_dim, G, R) */
+    SA_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_size query */
+    SA_ERR_INDEX = 4,         /* device saw an index outside [-1, N); it was skipped */
+    SA_ERR_TIMEOUT = 5,       /* a bounded device wait ran out; outputs are invalid */
+    SA_ERR_CUDA = 6           /* a CUDA runtime/driver call failed (no device, launch error) */
+} sa_status;
+
+typedef enum { SA_BF16 = 0, SA_F32 = 1 } sa_dtype;
+
+#define SA_HEADS 64
+#define SA_HEAD_DIM 512
+#define SA_MAX_K 2048
+
+/*
+ * Bytes of workspace `sa_sparse_attn` needs for this shape on the current
+ * device (the split-query partial results depend on its SM count).  Always a
+ * multiple of 256 and at least 256 (the error word).
+ */
+size_t sa_sparse_attn_workspace_size(int B, int T, int H, int D, int K);
+
+/*
+ * sparse_attn ("DeepSeek-V4.1 > Output projection" page, Attention.forward).
+ *   q      bf16 [B, T, H, D] contiguous, 16-byte aligned
+ *   kv     bf16 [B, N, D] contiguous, 16-byte aligned: per batch row the
+ *          window ring rows followed by the compressed rows
+ *   sink   fp32 [H]
+ *   idx    int32 [B, T, K] contiguous; values in [0, N) or -1 (skip)
+ *   scale  softmax scale applied to q.k (the pages use D ** -0.5)
+ *   out    [B, T, H, D] contiguous, 16-byte aligned, bf16 or fp32 (out_dtype)
+ *   workspace / ws_bytes: device scratch, 256-byte aligned, zeroed once
+ * Returns SA_OK once the work is enqueued.
+ */
+sa_status sa_sparse_attn(const void *q, const void *kv, const float *sink,
+                         const int32_t *idx, float scale, int B, int T, int H,
+                         int D, int N, int K, void *out, sa_dtype out_dtype,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Bytes of workspace `sa_sparse_attn_rope_wo_a` needs: the attention
+ * workspace plus the bf16 attention output [B, T, H, D] it keeps between the
+ * two steps.
+ */
+size_t sa_sparse_attn_rope_wo_a_workspace_size(int B, int T, int H, int D, int K,
+                                               int G, int R);
+
+/*
+ * sparse_attn, then the inverse rotary embedding of the last rope_dim
+ * features of every head (`apply_rotary_emb(o[..., -rd:], freqs_cis, True)`),
+ * then the grouped projection (`o.view(B, T, G, -1)` einsum
+ * `wo_a.weight.view(G, R, -1)`), all from the same page's Attention.forward.
+ *   (q, kv, sink, idx, scale, B, T, H, D, N, K) as for sa_sparse_attn
+ *   rope_cos_sin fp32 [T, rope_dim/2, 2]: row t holds (cos, sin) of
+ *          pos_t * w_i for the frequency pairs i of query t (same for every
+ *          batch row; see sa_rope_table).  Feature pair i is (D - rope_dim + 2i,
+ *          D - rope_dim + 2i + 1), rotated as one complex number by -pos_t*w_i.
+ *   rope_dim 64 (even, <= D)
+ *   wo_a   bf16 [G, R, H*D/G] contiguous, 16-byte aligned ([out, in] per group)
+ *   G, R   8 groups x 1024 rank on the fast path
+ *   out    bf16 [B, T, G*R] contiguous, 16-byte aligned
+ */
+sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *sink,
+                                   const int32_t *idx, float scale, int B, int T,
+                                   int H, int D, int N, int K,
+                                   const float *rope_cos_sin, int rope_dim,
+                                   const void *wo_a, int G, int R, void *out,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Host helper: fill cos_sin_host fp32 [T, rope_dim/2, 2] with
+ * (cos, sin)((start_pos + t) * theta ** (-2i / rope_dim)), computed in double.
+ * This is the precomputed rotary table of Attention.__init__ (plain theta, no
+ * long-context frequency correction).  Returns SA_ERR_INVALID_ARG on bad sizes.
+ */
+sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim,
+                        float *cos_sin_host);
+
+/*
+ * Synchronise `stream`, read the workspace error word, clear it, and return
+ * SA_ERR_TIMEOUT, SA_ERR_INDEX (in that order of precedence) or SA_OK.
+ */
+sa_status sa_check_errors(void *workspace, void *stream);
+
+/* Static description of a status code. */
+const char *sa_status_string(sa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_H_ */

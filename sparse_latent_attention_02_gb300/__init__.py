@@ -1,0 +1,214 @@
+"""GB300-native sparse latent attention (DeepSeek-V4.1 ``sparse_attn`` step).
+
+A thin ctypes binding over ``libsa.so`` (the C ABI of ``include/sa.h``); every
+step of the computation runs in the library's sm_103a kernels.  PyTorch only
+supplies device memory and the current stream.  When the library is missing
+or no GPU is present, the calls raise -- there is no fallback.
+
+    out = sparse_attn(q, kv, sink, idx, scale)            # bf16 [B,T,64,512]
+    y   = sparse_attn_rope_wo_a(q, kv, sink, idx, scale, rope_cos_sin, wo_a)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from ._build import LIB as _LIB_PATH, build  # noqa: F401
+
+__all__ = ["sparse_attn", "sparse_attn_rope_wo_a", "rope_table", "workspace_size",
+           "fused_workspace_size", "check_errors", "SAError", "library", "build"]
+
+HEADS, HEAD_DIM, MAX_K = 64, 512, 2048
+_STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_WORKSPACE",
+           4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA"}
+EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn",
+           "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
+           "sa_rope_table", "sa_check_errors", "sa_status_string")
+
+
+class SAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        msg = library().sa_status_string(int(code)).decode()
+        super().__init__(f"{where}: {_STATUS.get(int(code), code)} ({msg})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library(path: str | None = None) -> ctypes.CDLL:
+    """Load ``libsa.so`` (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None or path is not None:
+            p = path or _LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build the CUDA library first "
+                                   "(sparse_latent_attention_02_gb300.build())")
+            lib = ctypes.CDLL(p)
+            V, I, F, D, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_size_t
+            lib.sa_sparse_attn_workspace_size.restype = Z
+            lib.sa_sparse_attn_workspace_size.argtypes = [I, I, I, I, I]
+            lib.sa_sparse_attn.restype = I
+            lib.sa_sparse_attn.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, Z, V]
+            lib.sa_sparse_attn_rope_wo_a_workspace_size.restype = Z
+            lib.sa_sparse_attn_rope_wo_a_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            lib.sa_sparse_attn_rope_wo_a.restype = I
+            lib.sa_sparse_attn_rope_wo_a.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
+                                                     V, V, Z, V]
+            lib.sa_rope_table.restype = I
+            lib.sa_rope_table.argtypes = [D, I, I, I, V]
+            lib.sa_check_errors.restype = I
+            lib.sa_check_errors.argtypes = [V, V]
+            lib.sa_status_string.restype = ctypes.c_char_p
+            lib.sa_status_string.argtypes = [I]
+            if path is None:
+                _lib = lib
+            else:
+                return lib
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SAError(code, where)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device: torch.device, key: str) -> torch.Tensor:
+    """A zero-initialised per-device scratch buffer, grown on demand."""
+    k = (device.index, key)
+    ws = _ws_cache.get(k)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[k] = ws
+    return ws
+
+
+def workspace_size(B: int, T: int, K: int) -> int:
+    return int(library().sa_sparse_attn_workspace_size(B, T, HEADS, HEAD_DIM, K))
+
+
+def fused_workspace_size(B: int, T: int, K: int, G: int, R: int) -> int:
+    return int(library().sa_sparse_attn_rope_wo_a_workspace_size(B, T, HEADS, HEAD_DIM, K, G, R))
+
+
+def _attn_args(q, kv, sink, idx):
+    _need(q, "q", torch.bfloat16, 4)
+    _need(kv, "kv", torch.bfloat16, 3)
+    _need(sink, "sink", torch.float32, 1)
+    _need(idx, "idx", torch.int32, 3)
+    B, T, H, D = q.shape
+    if kv.shape[0] != B or kv.shape[2] != D:
+        raise ValueError(f"kv {tuple(kv.shape)} does not match q {tuple(q.shape)}")
+    if sink.shape[0] != H or idx.shape[:2] != (B, T):
+        raise ValueError("sink / idx shapes do not match q")
+    devs = {t.device for t in (q, kv, sink, idx)}
+    if len(devs) != 1:
+        raise ValueError("all inputs must be on one device")
+    return B, T, H, D, kv.shape[1], idx.shape[2]
+
+
+def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torch.Tensor,
+                scale: float, out: torch.Tensor | None = None,
+                out_dtype: torch.dtype = torch.bfloat16, workspace: torch.Tensor | None = None,
+                stream=None, check: bool = False) -> torch.Tensor:
+    """``sparse_attn(q, kv, attn_sink, topk_idxs, softmax_scale)`` -> [B, T, H, D].
+
+    q bf16 [B,T,64,512], kv bf16 [B,N,512], sink fp32 [64], idx int32 [B,T,K].
+    ``check=True`` synchronises and raises on a device-side error (bad index).
+    """
+    B, T, H, D, N, K = _attn_args(q, kv, sink, idx)
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=out_dtype, device=q.device)
+    else:
+        _need(out, "out", out.dtype, 4)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    lib = library()
+    need = int(lib.sa_sparse_attn_workspace_size(B, T, H, D, K))
+    if workspace is None:
+        workspace = _workspace(need, q.device, "attn")
+    code = lib.sa_sparse_attn(q.data_ptr(), kv.data_ptr(), sink.data_ptr(), idx.data_ptr(),
+                              float(scale), B, T, H, D, N, K, out.data_ptr(),
+                              1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check(code, "sa_sparse_attn")
+    if check:
+        check_errors(workspace, stream)
+    return out
+
+
+def sparse_attn_rope_wo_a(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor,
+                          idx: torch.Tensor, scale: float, rope_cos_sin: torch.Tensor,
+                          wo_a: torch.Tensor, out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None, stream=None,
+                          check: bool = False) -> torch.Tensor:
+    """sparse_attn, inverse RoPE on the last rope_dim features, grouped wo_a.
+
+    rope_cos_sin fp32 [T, rope_dim/2, 2]; wo_a bf16 [G, R, H*D/G]; returns bf16 [B, T, G*R].
+    """
+    B, T, H, D, N, K = _attn_args(q, kv, sink, idx)
+    _need(rope_cos_sin, "rope_cos_sin", torch.float32, 3)
+    _need(wo_a, "wo_a", torch.bfloat16, 3)
+    G, R, Din = wo_a.shape
+    if rope_cos_sin.shape[0] != T or rope_cos_sin.shape[2] != 2:
+        raise ValueError("rope_cos_sin must be [T, rope_dim/2, 2]")
+    if G * Din != H * D:
+        raise ValueError("wo_a must be [G, R, H*D/G]")
+    rope_dim = 2 * rope_cos_sin.shape[1]
+    if out is None:
+        out = torch.empty((B, T, G * R), dtype=torch.bfloat16, device=q.device)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+    lib = library()
+    need = int(lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, H, D, K, G, R))
+    if workspace is None:
+        workspace = _workspace(need, q.device, "fused")
+    code = lib.sa_sparse_attn_rope_wo_a(q.data_ptr(), kv.data_ptr(), sink.data_ptr(),
+                                        idx.data_ptr(), float(scale), B, T, H, D, N, K,
+                                        rope_cos_sin.data_ptr(), rope_dim, wo_a.data_ptr(), G, R,
+                                        out.data_ptr(), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream_ptr(stream))
+    _check(code, "sa_sparse_attn_rope_wo_a")
+    if check:
+        check_errors(workspace, stream)
+    return out
+
+
+def rope_table(theta: float, start_pos: int, T: int, rope_dim: int = 64) -> torch.Tensor:
+    """Host-built fp32 [T, rope_dim/2, 2] (cos, sin) table (double-precision angles)."""
+    t = torch.empty((T, rope_dim // 2, 2), dtype=torch.float32)
+    _check(library().sa_rope_table(float(theta), int(start_pos), int(T), int(rope_dim),
+                                   t.data_ptr() if T > 0 else None), "sa_rope_table")
+    return t
+
+
+def check_errors(workspace: torch.Tensor, stream=None):
+    """Synchronise, read and clear the workspace error word; raise SAError if set."""
+    _check(library().sa_check_errors(workspace.data_ptr(), _stream_ptr(stream)), "device")

@@ -1,0 +1,296 @@
+// sa_api.cu -- the C ABI of include/sa.h: argument checks, workspace layout,
+// tensor-map encoding and kernel launches.  No torch types cross this boundary.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "sa_internal.h"
+
+namespace sa {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Bound on every device-side wait.  A stage normally waits microseconds; a
+// second means the pipeline is stuck.  SA_WAIT_TIMEOUT_MS overrides it.
+uint64_t wait_timeout_ns()
+{
+    static uint64_t ns = [] {
+        const char *e = std::getenv("SA_WAIT_TIMEOUT_MS");
+        long ms = e ? std::strtol(e, nullptr, 10) : 0;
+        if (ms <= 0)
+            ms = 1000;
+        return (uint64_t)ms * 1000000ull;
+    }();
+    return ns;
+}
+
+bool current_sms(int *sms)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && *sms > 0;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks shared by both attention entry points.  Sets *nothing_to_do when the
+// call has no output elements.
+sa_status check_attn_args(const void *q, const void *kv, const float *sink, const int32_t *idx,
+                          float scale, int B, int T, int H, int D, int N, int K, const void *out,
+                          const void *ws)
+{
+    if (B < 0 || T < 0 || H < 0 || D < 0 || N < 0 || K < 0)
+        return SA_ERR_INVALID_ARG;
+    if (H != SA_HEADS || D != SA_HEAD_DIM || K > SA_MAX_K)
+        return SA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale))
+        return SA_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 256))
+        return SA_ERR_INVALID_ARG;
+    if ((int64_t)B * T == 0)
+        return SA_OK;
+    if ((int64_t)B * T * H >= (int64_t)1 << 31 || (int64_t)B * N >= (int64_t)1 << 31)
+        return SA_ERR_UNSUPPORTED;
+    if (!out || !aligned(out, 16))
+        return SA_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!q || !aligned(q, 16) || !sink || !idx || !aligned(idx, 4))
+            return SA_ERR_INVALID_ARG;
+        if (N > 0 && (!kv || !aligned(kv, 16)))
+            return SA_ERR_INVALID_ARG;
+    }
+    return SA_OK;
+}
+
+sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const float *sink,
+                           const int32_t *idx, float scale, int B, int T, int N, int K, void *out,
+                           bool out_f32, void *ws)
+{
+    std::memset(&p, 0, sizeof p);
+    const uint64_t rows = (uint64_t)B * T * SA_HEADS;
+    if (!encode_tmap_2d(&p.tm_q, q, rows, SA_HEAD_DIM, 64, 64))
+        return SA_ERR_CUDA;
+    p.kv = static_cast<const uint16_t *>(kv);
+    p.idx = idx;
+    p.sink = sink;
+    p.out = out;
+    p.err = static_cast<uint32_t *>(ws);
+    p.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + WS_HEADER);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.BT = (int64_t)B * T;
+    p.T = T;
+    p.N = N;
+    p.K = K;
+    p.out_f32 = out_f32 ? 1 : 0;
+    p.timeout_ns = wait_timeout_ns();
+    return SA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows)
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult qr{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace sa
+
+using namespace sa;
+
+extern "C" {
+
+size_t sa_sparse_attn_workspace_size(int B, int T, int H, int D, int K)
+{
+    (void)H;
+    (void)D;
+    int sms = 0;
+    if (!current_sms(&sms))
+        sms = 1;
+    if (B < 0 || T < 0 || K < 0)
+        return WS_HEADER;
+    return attn_workspace_bytes((int64_t)B * T, K, sms);
+}
+
+sa_status sa_sparse_attn(const void *q, const void *kv, const float *sink, const int32_t *idx,
+                         float scale, int B, int T, int H, int D, int N, int K, void *out,
+                         sa_dtype out_dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
+    if (st != SA_OK)
+        return st;
+    if (out_dtype != SA_BF16 && out_dtype != SA_F32)
+        return SA_ERR_INVALID_ARG;
+    const int64_t BT = (int64_t)B * T;
+    if (BT == 0)
+        return SA_OK;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
+    if (ws_bytes < attn_workspace_bytes(BT, K, sms))
+        return SA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t esz = out_dtype == SA_F32 ? 4 : 2;
+    if (K == 0)
+        return cudaMemsetAsync(out, 0, (size_t)BT * H * D * esz, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+    AttnParams p;
+    st = fill_attn_params(p, q, kv, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
+    if (st != SA_OK)
+        return st;
+    const Schedule sch = attn_schedule(BT, K, sms);
+    return launch_attention(p, sch, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+size_t sa_sparse_attn_rope_wo_a_workspace_size(int B, int T, int H, int D, int K, int G, int R)
+{
+    (void)G;
+    (void)R;
+    const size_t attn = sa_sparse_attn_workspace_size(B, T, H, D, K);
+    if (B < 0 || T < 0 || H < 0 || D < 0)
+        return attn;
+    return round256(attn) + round256((size_t)B * T * H * D * 2);
+}
+
+sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *sink,
+                                   const int32_t *idx, float scale, int B, int T, int H, int D,
+                                   int N, int K, const float *rope_cos_sin, int rope_dim,
+                                   const void *wo_a, int G, int R, void *out, void *workspace,
+                                   size_t ws_bytes, void *stream)
+{
+    sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
+    if (st != SA_OK)
+        return st;
+    if (G <= 0 || R <= 0 || rope_dim < 0)
+        return SA_ERR_INVALID_ARG;
+    if ((H * D) % G != 0 || ((H * D) / G) % 64 != 0 || R % 256 != 0 || rope_dim % 4 != 0 ||
+        rope_dim > D)
+        return SA_ERR_UNSUPPORTED;
+    const int64_t BT = (int64_t)B * T;
+    if (BT == 0)
+        return SA_OK;
+    if (!wo_a || !aligned(wo_a, 16) || (rope_dim > 0 && !rope_cos_sin))
+        return SA_ERR_INVALID_ARG;
+    if (BT >= ((int64_t)1 << 31) / 128)
+        return SA_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
+    const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
+    const size_t o_bytes = round256((size_t)BT * H * D * 2);
+    if (ws_bytes < attn_ws + o_bytes)
+        return SA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *o = static_cast<uint8_t *>(workspace) + attn_ws;
+
+    // 1) sparse attention with the inverse rotary embedding fused into its
+    //    epilogue, bf16 output kept in the workspace
+    if (K == 0) {
+        if (cudaMemsetAsync(o, 0, (size_t)BT * H * D * 2, s) != cudaSuccess)
+            return SA_ERR_CUDA;
+    } else {
+        AttnParams p;
+        st = fill_attn_params(p, q, kv, sink, idx, scale, B, T, N, K, o, false, workspace);
+        if (st != SA_OK)
+            return st;
+        p.rope = rope_cos_sin;
+        p.rope_dim = rope_dim;
+        const Schedule sch = attn_schedule(BT, K, sms);
+        if (launch_attention(p, sch, s) != cudaSuccess)
+            return SA_ERR_CUDA;
+    }
+
+    // 2) grouped wo_a
+    GemmParams g;
+    std::memset(&g, 0, sizeof g);
+    const int Din = H * D / G;
+    if (!encode_tmap_2d(&g.tm_a, o, (uint64_t)BT, (uint64_t)H * D, 64, 128) ||
+        !encode_tmap_2d(&g.tm_b, wo_a, (uint64_t)G * R, (uint64_t)Din, 64, 256))
+        return SA_ERR_CUDA;
+    g.y = static_cast<uint16_t *>(out);
+    g.err = static_cast<uint32_t *>(workspace);
+    g.M = (int)BT;
+    g.G = G;
+    g.R = R;
+    g.Din = Din;
+    g.timeout_ns = wait_timeout_ns();
+    return launch_wo_a(g, sms, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim, float *cos_sin_host)
+{
+    if (T < 0 || rope_dim <= 0 || rope_dim % 2 != 0 || !(theta > 0.0) || start_pos < 0)
+        return SA_ERR_INVALID_ARG;
+    if (T > 0 && !cos_sin_host)
+        return SA_ERR_INVALID_ARG;
+    const int half = rope_dim / 2;
+    for (int t = 0; t < T; ++t) {
+        const double pos = (double)start_pos + t;
+        for (int i = 0; i < half; ++i) {
+            const double ang = pos * std::pow(theta, -2.0 * i / rope_dim);
+            cos_sin_host[((size_t)t * half + i) * 2] = (float)std::cos(ang);
+            cos_sin_host[((size_t)t * half + i) * 2 + 1] = (float)std::sin(ang);
+        }
+    }
+    return SA_OK;
+}
+
+sa_status sa_check_errors(void *workspace, void *stream)
+{
+    if (!workspace)
+        return SA_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SA_ERR_CUDA;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, workspace, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (w) {
+        const uint32_t z = 0;
+        if (cudaMemcpy(workspace, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess)
+            return SA_ERR_CUDA;
+    }
+    if (w & ERRBIT_TIMEOUT)
+        return SA_ERR_TIMEOUT;
+    if (w & ERRBIT_INDEX)
+        return SA_ERR_INDEX;
+    return SA_OK;
+}
+
+const char *sa_status_string(sa_status s)
+{
+    switch (s) {
+    case SA_OK: return "ok";
+    case SA_ERR_INVALID_ARG: return "invalid argument (null, negative or misaligned)";
+    case SA_ERR_UNSUPPORTED: return "shape outside the supported fast path";
+    case SA_ERR_WORKSPACE: return "workspace too small";
+    case SA_ERR_INDEX: return "an index outside [-1, N) was seen and skipped";
+    case SA_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case SA_ERR_CUDA: return "CUDA runtime or driver error";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

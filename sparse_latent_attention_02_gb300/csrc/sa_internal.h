@@ -1,0 +1,69 @@
+// sa_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sa.h"
+
+namespace sa {
+
+// Bits of the device error word (first 4 bytes of every workspace).
+constexpr uint32_t ERRBIT_INDEX = 1u;
+constexpr uint32_t ERRBIT_TIMEOUT = 2u;
+
+// Workspace layout: [0, 256) header (error word), then the split partials.
+constexpr size_t WS_HEADER = 256;
+// One split partial: unnormalised O [64 heads][512] fp32, then m[64], l[64].
+constexpr int PART_O = 64 * 512;
+constexpr int PART_STRIDE = PART_O + 128;
+
+struct AttnParams {
+    CUtensorMap tm_q;          // q as 2-D [B*T*H rows, D cols] bf16, box 64x64, 128B swizzle
+    const uint16_t *kv;        // bf16 [B, N, D]
+    const int32_t *idx;        // int32 [B*T, K]
+    const float *sink;         // fp32 [H]
+    void *out;                 // [B*T, H, D] bf16 or fp32
+    float *part;               // split partials (workspace)
+    uint32_t *err;             // error word (workspace)
+    const float *rope;         // fp32 [T, rope_dim/2, 2] or null
+    float scale_log2;          // softmax scale * log2(e)
+    int64_t BT;                // B * T
+    int T, N, K;
+    int out_f32;
+    int split;                 // 0: whole queries, CTA i takes i, i+grid, ...; 1: entry ranges
+    int64_t per_cta;           // split: raw list entries per CTA
+    int rope_dim;              // 0 = no rotary epilogue
+    uint64_t timeout_ns;       // bound on every device-side wait
+};
+
+struct Schedule {
+    int grid;
+    int split;
+    int64_t per_cta;
+};
+
+// Decide the grid and the split of the index lists for this shape and device.
+Schedule attn_schedule(int64_t BT, int K, int num_sms);
+size_t attn_workspace_bytes(int64_t BT, int K, int num_sms);
+
+// Enqueue the attention kernel (and the split combine when needed).
+cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st);
+
+struct GemmParams {
+    CUtensorMap tm_a;          // o as 2-D [M rows, G*Din cols] bf16, box 64x128
+    CUtensorMap tm_b;          // W as 2-D [G*R rows, Din cols] bf16, box 64x256
+    uint16_t *y;               // bf16 [M, G*R]
+    uint32_t *err;
+    int M, G, R, Din;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st);
+
+// Encode a 2-D bf16 tensor map (row-major [rows, cols], 128B swizzle).
+bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows);
+
+}  // namespace sa

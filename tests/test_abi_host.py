@@ -1,0 +1,127 @@
+"""The C-ABI library builds, loads and rejects bad arguments on the host
+(CPU only: no call here reaches a kernel)."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import sparse_latent_attention_02_gb300 as sa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "sa.h")
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sa.build()
+    return sa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(sa.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.sa_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.sa_status_string(99).decode() == "unknown status"
+
+
+def _attn(lib, **kw):
+    a = dict(q=16, kv=16, sink=16, idx=16, scale=0.1, B=1, T=1, H=64, D=512, N=8, K=4,
+             out=16, dt=0, ws=256, wsb=1 << 20, stream=None)
+    a.update(kw)
+    return lib.sa_sparse_attn(a["q"], a["kv"], a["sink"], a["idx"], a["scale"], a["B"], a["T"],
+                              a["H"], a["D"], a["N"], a["K"], a["out"], a["dt"], a["ws"],
+                              a["wsb"], a["stream"])
+
+
+def test_host_argument_checks(lib):
+    # these are rejected before any CUDA call (pointers are never dereferenced)
+    assert _attn(lib, H=32) == UNSUPPORTED
+    assert _attn(lib, D=256) == UNSUPPORTED
+    assert _attn(lib, K=sa.MAX_K + 1) == UNSUPPORTED
+    assert _attn(lib, B=-1) == INVALID
+    assert _attn(lib, K=-3) == INVALID
+    assert _attn(lib, ws=None) == INVALID
+    assert _attn(lib, ws=128) == INVALID          # workspace must be 256-byte aligned
+    assert _attn(lib, out=None) == INVALID
+    assert _attn(lib, out=8) == INVALID           # output must be 16-byte aligned
+    assert _attn(lib, q=None) == INVALID
+    assert _attn(lib, kv=24) == INVALID
+    assert _attn(lib, idx=2) == INVALID
+    assert _attn(lib, sink=None) == INVALID
+    assert _attn(lib, scale=float("nan")) == INVALID
+    assert _attn(lib, dt=7) in (INVALID, 6)      # bad dtype (or no device to query)
+    # empty problems are fine and touch nothing
+    assert _attn(lib, B=0, q=None, out=None) == OK
+    assert _attn(lib, T=0) == OK
+
+
+def test_fused_argument_checks(lib):
+    def call(**kw):
+        a = dict(q=16, kv=16, sink=16, idx=16, scale=0.1, B=1, T=1, H=64, D=512, N=8, K=4,
+                 rope=16, rope_dim=64, w=16, G=8, R=1024, out=16, ws=256, wsb=1 << 30,
+                 stream=None)
+        a.update(kw)
+        return lib.sa_sparse_attn_rope_wo_a(a["q"], a["kv"], a["sink"], a["idx"], a["scale"],
+                                            a["B"], a["T"], a["H"], a["D"], a["N"], a["K"],
+                                            a["rope"], a["rope_dim"], a["w"], a["G"], a["R"],
+                                            a["out"], a["ws"], a["wsb"], a["stream"])
+    assert call(G=0) == INVALID
+    assert call(G=3) == UNSUPPORTED               # 64*512 not divisible into 64-multiples
+    assert call(R=1000) == UNSUPPORTED
+    assert call(rope_dim=6) == UNSUPPORTED
+    assert call(rope_dim=1024) == UNSUPPORTED
+    assert call(w=None) == INVALID
+    assert call(rope=None) == INVALID
+    assert call(H=16) == UNSUPPORTED
+
+
+def test_workspace_size_queries(lib):
+    # without a device the size falls back to one SM; it is always >= 256, 256-aligned
+    for B, T, K in [(1, 16, 192), (64, 1, 640), (1, 8192, 640), (0, 0, 0)]:
+        n = lib.sa_sparse_attn_workspace_size(B, T, 64, 512, K)
+        assert n >= 256 and n % 256 == 0
+        f = lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, 64, 512, K, 8, 1024)
+        assert f >= n + B * T * 64 * 512 * 2
+
+
+def test_rope_table_host_helper(lib):
+    t = sa.rope_table(160000.0, 3, 5, 64).numpy().astype(np.float64)
+    assert t.shape == (5, 32, 2)
+    for tt in range(5):
+        for i in range(32):
+            ang = (3 + tt) * 160000.0 ** (-2.0 * i / 64)
+            assert abs(t[tt, i, 0] - math.cos(ang)) < 1e-7
+            assert abs(t[tt, i, 1] - math.sin(ang)) < 1e-7
+    assert lib.sa_rope_table(160000.0, 0, 4, 63, None) == INVALID
+    assert lib.sa_rope_table(-1.0, 0, 4, 64, None) == INVALID
+
+
+def test_check_errors_rejects_null(lib):
+    assert lib.sa_check_errors(None, None) == INVALID
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 64, 512, dtype=torch.bfloat16)
+    kv = torch.zeros(1, 4, 512, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sa.sparse_attn(q, kv, torch.zeros(64), torch.zeros(1, 1, 4, dtype=torch.int32), 0.1)
+    with pytest.raises(TypeError):
+        sa.sparse_attn(q.float(), kv, torch.zeros(64), torch.zeros(1, 1, 4, dtype=torch.int32), 0.1)
