@@ -150,12 +150,12 @@ def make_sets(wl: I.Workload, n_sets: int, seed: int, dev) -> list:
     return [I.make_inputs(wl, seed=seed + 17 * i, device=dev) for i in range(n_sets)]
 
 
-def sets_for(wl: I.Workload, dev, seed=0, min_sets=2) -> list:
+def sets_for(wl: I.Workload, dev, seed=0, min_sets=2, n_sets=None) -> list:
     """Enough independent input sets that one rotation touches > 2x L2."""
     probe = I.make_inputs(wl, seed=seed, device=dev)
     a = algorithmic(wl, probe["idx"])
     n = max(min_sets, int(np.ceil(2.5 * l2_bytes() / max(a["bytes"], 1))))
-    n = min(n, 8)
+    n = min(n, 8) if n_sets is None else n_sets
     return [probe] + make_sets(wl, n - 1, seed + 1, dev)
 
 
@@ -193,10 +193,17 @@ def time_graph_steps(step_fns, steps: int, warmup: int):
 
 # ------------------------------------------------------------------ our arm
 
-def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, sampler=None):
+def launches_per_call(wl: I.Workload, num_sms: int) -> int:
+    """Kernels one call enqueues: the attention kernel, plus the piece combine
+    when there are fewer queries than SMs, plus the grouped GEMM of the tail."""
+    n = 1 + (1 if wl.n_queries < num_sms and wl.K > 0 else 0)
+    return n + (1 if wl.tail else 0)
+
+
+def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_sets=None):
     import sparse_latent_attention_02_gb300 as sa
     wl = I.WORKLOADS[name]
-    sets = sets_for(wl, dev)
+    sets = sets_for(wl, dev, n_sets=n_sets)
     outs = []
     fns = []
     if wl.tail:
@@ -232,6 +239,8 @@ def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, samp
         "bytes_per_step": int(per_step_bytes), "flops_per_step": int(per_step_flops),
         "valid_pairs_per_step": int(np.mean([w["pairs"] for w in work])),
         "window": (t0, t1),
+        "gpu_launches": steps * launches_per_call(
+            wl, torch.cuda.get_device_properties(dev).multi_processor_count),
     }
     if with_e2e:
         res["e2e"] = bench_e2e(wl, sets[0], steps, warmup, dev)
@@ -305,7 +314,8 @@ def run_ours(args):
     sampler = ClockSampler(0)
     sampler.start()
     time.sleep(0.3)
-    head = bench_workload(HEADLINE, args.steps, args.warmup, dev, with_e2e=True)
+    head = bench_workload(args.workload, args.steps, args.warmup, dev, with_e2e=not args.no_e2e,
+                          n_sets=args.sets)
     clocks = sampler.summary(*head.pop("window"))
     extra = {}
     if not args.headline_only:
@@ -324,14 +334,14 @@ def run_ours(args):
                                  "peak_note": f"{pk['source']} HBM copy"}
             extra[name] = r
     sampler.stop()
-    e2e = head.pop("e2e")
-    cpu = cpu_baseline(HEADLINE, budget_s=args.cpu_seconds)
+    e2e = head.pop("e2e", None)
+    cpu = cpu_baseline(args.workload, budget_s=args.cpu_seconds) if args.cpu_seconds > 0 else None
     line = {
         "metric": METRIC, "value": head["queries_per_s"], "unit": "queries/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{HEADLINE}: B={head['B']} T={head['T']} H=64 D=512 "
+        "config": {"workload": f"{args.workload}: B={head['B']} T={head['T']} H=64 D=512 "
                                f"N={head['N']} K={head['K']}",
                    "parallelism": "replicas only (one GPU)",
                    "l2": f"inputs rotate over {head['input_sets']} independent sets "
@@ -344,7 +354,7 @@ def run_ours(args):
                      "note": f"peak = {pk['source']} HBM copy; achieved = algorithmic bytes "
                              f"({head['bytes_per_step']} per call) / call duration"},
         "e2e": e2e,
-        "gpu_launches": None,
+        "gpu_launches": head["gpu_launches"],
         "clocks": clocks,
         "cpu_baseline": cpu,
         "workloads": extra,
@@ -385,7 +395,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU-baseline budget; 0 skips it (profiling runs)")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(I.WORKLOADS),
+                    help="workload of the headline line (default: decode)")
+    ap.add_argument("--sets", type=int, default=None,
+                    help="number of rotating input sets (default: enough for > 2x L2)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
