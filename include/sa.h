@@ -124,6 +124,36 @@ sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim,
                         float *cos_sin_host);
 
 /*
+ * sa_sparse_attn without a workspace argument, for callers that cannot
+ * allocate device memory where they run attention (an allocator or memory-pool
+ * callback, a plugin whose host framework owns every device allocation, a
+ * real-time loop that must not enter the driver's allocator).  The pages have
+ * no counterpart: this is a convenience of this library.
+ *
+ * The scratch is a 40 MiB array in the library's device image: every process
+ * that loads the library holds it on every GPU it uses, until exit.  Shapes
+ * whose scratch (sa_sparse_attn_workspace_size) exceeds 40 MiB return
+ * SA_ERR_WORKSPACE before anything is enqueued; on GB300 every shape
+ * sa_sparse_attn accepts fits.  Nothing is allocated: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents: each call zeroes its error word (enqueued on `stream` before the
+ * kernels), so calls whose work overlaps on the GPU race and must not be
+ * issued on different streams at the same time.
+ *
+ * Arguments as for sa_sparse_attn, without workspace/ws_bytes.  If scratch_out
+ * is not NULL it receives the array's device address; pass it to
+ * sa_check_errors to read this call's device-side error report.
+ */
+sa_status sa_sparse_attn_noalloc(const void *q, const void *kv, const float *sink,
+                                 const int32_t *idx, float scale, int B, int T, int H,
+                                 int D, int N, int K, void *out, sa_dtype out_dtype,
+                                 void **scratch_out, void *stream);
+
+/*
  * Synchronise `stream`, read the workspace error word, clear it, and return
  * SA_ERR_TIMEOUT, SA_ERR_INDEX (in that order of precedence) or SA_OK.
  */

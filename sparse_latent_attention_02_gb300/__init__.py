@@ -26,7 +26,7 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_
            4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA"}
 EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn",
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
-           "sa_rope_table", "sa_check_errors", "sa_status_string")
+           "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc")
 
 
 class SAError(RuntimeError):
@@ -66,6 +66,9 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_check_errors.argtypes = [V, V]
             lib.sa_status_string.restype = ctypes.c_char_p
             lib.sa_status_string.argtypes = [I]
+            lib.sa_sparse_attn_noalloc.restype = I
+            lib.sa_sparse_attn_noalloc.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I,
+                                                   ctypes.POINTER(ctypes.c_void_p), V]
             if path is None:
                 _lib = lib
             else:

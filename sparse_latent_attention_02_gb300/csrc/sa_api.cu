@@ -39,35 +39,6 @@ bool current_sms(int *sms)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Checks shared by both attention entry points.  Sets *nothing_to_do when the
-// call has no output elements.
-sa_status check_attn_args(const void *q, const void *kv, const float *sink, const int32_t *idx,
-                          float scale, int B, int T, int H, int D, int N, int K, const void *out,
-                          const void *ws)
-{
-    if (B < 0 || T < 0 || H < 0 || D < 0 || N < 0 || K < 0)
-        return SA_ERR_INVALID_ARG;
-    if (H != SA_HEADS || D != SA_HEAD_DIM || K > SA_MAX_K)
-        return SA_ERR_UNSUPPORTED;
-    if (!std::isfinite(scale))
-        return SA_ERR_INVALID_ARG;
-    if (!ws || !aligned(ws, 256))
-        return SA_ERR_INVALID_ARG;
-    if ((int64_t)B * T == 0)
-        return SA_OK;
-    if ((int64_t)B * T * H >= (int64_t)1 << 31 || (int64_t)B * N >= (int64_t)1 << 31)
-        return SA_ERR_UNSUPPORTED;
-    if (!out || !aligned(out, 16))
-        return SA_ERR_INVALID_ARG;
-    if (K > 0) {
-        if (!q || !aligned(q, 16) || !sink || !idx || !aligned(idx, 4))
-            return SA_ERR_INVALID_ARG;
-        if (N > 0 && (!kv || !aligned(kv, 16)))
-            return SA_ERR_INVALID_ARG;
-    }
-    return SA_OK;
-}
-
 sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const float *sink,
                            const int32_t *idx, float scale, int B, int T, int N, int K, void *out,
                            bool out_f32, void *ws)
@@ -95,6 +66,34 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const f
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
+
+// Checks shared by the attention entry points; nothing is enqueued before them.
+sa_status check_attn_args(const void *q, const void *kv, const float *sink, const int32_t *idx,
+                          float scale, int B, int T, int H, int D, int N, int K, const void *out,
+                          const void *ws)
+{
+    if (B < 0 || T < 0 || H < 0 || D < 0 || N < 0 || K < 0)
+        return SA_ERR_INVALID_ARG;
+    if (H != SA_HEADS || D != SA_HEAD_DIM || K > SA_MAX_K)
+        return SA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale))
+        return SA_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 256))
+        return SA_ERR_INVALID_ARG;
+    if ((int64_t)B * T == 0)
+        return SA_OK;
+    if ((int64_t)B * T * H >= (int64_t)1 << 31 || (int64_t)B * N >= (int64_t)1 << 31)
+        return SA_ERR_UNSUPPORTED;
+    if (!out || !aligned(out, 16))
+        return SA_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!q || !aligned(q, 16) || !sink || !idx || !aligned(idx, 4))
+            return SA_ERR_INVALID_ARG;
+        if (N > 0 && (!kv || !aligned(kv, 16)))
+            return SA_ERR_INVALID_ARG;
+    }
+    return SA_OK;
+}
 
 bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint32_t box_cols, uint32_t box_rows)

@@ -62,6 +62,11 @@ struct GemmParams {
 
 cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st);
 
+// Host argument checks of the attention entry points (no CUDA call).
+sa_status check_attn_args(const void *q, const void *kv, const float *sink, const int32_t *idx,
+                          float scale, int B, int T, int H, int D, int N, int K, const void *out,
+                          const void *ws);
+
 // Encode a 2-D bf16 tensor map (row-major [rows, cols], 128B swizzle).
 bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint32_t box_cols, uint32_t box_rows);
