@@ -159,10 +159,40 @@ def sets_for(wl: I.Workload, dev, seed=0, min_sets=2, n_sets=None) -> list:
     return [probe] + make_sets(wl, n - 1, seed + 1, dev)
 
 
+# ------------------------------------------------------------------ ranks
+
+def dist_env():
+    """(rank, world, local_rank) from the torchrun environment (1 process if unset)."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_over_ranks(local_seconds: float, local_units: float):
+    """Whole-job throughput of independent replicas: the slowest rank's time
+    (max over ranks) and the units all ranks processed (sum)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return local_seconds, local_units
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def time_graph_steps(step_fns, steps: int, warmup: int):
     """Capture `steps` calls (rotating over step_fns) into one CUDA graph, warm
     up with a `warmup`-step graph, then time one replay with CUDA events on
-    the capturing stream.  Returns seconds for the `steps` calls."""
+    the capturing stream, between barriers across ranks.  Returns seconds for
+    the `steps` calls."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -182,11 +212,14 @@ def time_graph_steps(step_fns, steps: int, warmup: int):
         gw.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        barrier()
         t0 = time.time()
         e0.record(s)
         g.replay()
         e1.record(s)
         e1.synchronize()
+        torch.cuda.synchronize()
+        barrier()
         t1 = time.time()
     return e0.elapsed_time(e1) / 1e3, (t0, t1)
 
@@ -307,18 +340,29 @@ def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
 
 def run_ours(args):
     import sparse_latent_attention_02_gb300 as sa
-    sa.build()
-    dev = torch.device("cuda", 0)
+    rank, world, local = dist_env()
+    if rank == 0:
+        sa.build()
+    barrier()
+    dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
-    sampler = ClockSampler(0)
+    sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    head = bench_workload(args.workload, args.steps, args.warmup, dev, with_e2e=not args.no_e2e,
-                          n_sets=args.sets)
+    head = bench_workload(args.workload, args.steps, args.warmup, dev,
+                          with_e2e=not args.no_e2e and world == 1, n_sets=args.sets)
+    secs, units = aggregate_over_ranks(head["ms_per_step"] * 1e-3 * args.steps,
+                                       head["queries_per_s"] * head["ms_per_step"] * 1e-3 * args.steps)
+    head["job_queries_per_s"] = units / secs
+    head["job_ms_per_step"] = secs / args.steps * 1e3
     clocks = sampler.summary(*head.pop("window"))
+    if rank != 0:
+        sampler.stop()
+        barrier()
+        return
     extra = {}
-    if not args.headline_only:
+    if not args.headline_only and world == 1:
         for name in ("long_decode", "prefill", "fused_tail"):
             steps = max(3, min(args.steps, 20))
             r = bench_workload(name, steps, max(args.warmup, 3), dev, with_e2e=False)
@@ -335,15 +379,17 @@ def run_ours(args):
             extra[name] = r
     sampler.stop()
     e2e = head.pop("e2e", None)
-    cpu = cpu_baseline(args.workload, budget_s=args.cpu_seconds) if args.cpu_seconds > 0 else None
+    cpu = (cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+           if args.cpu_seconds > 0 and world == 1 else None)
     line = {
-        "metric": METRIC, "value": head["queries_per_s"], "unit": "queries/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["job_queries_per_s"], "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["job_ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: B={head['B']} T={head['T']} H=64 D=512 "
                                f"N={head['N']} K={head['K']}",
-                   "parallelism": "replicas only (one GPU)",
+                   "parallelism": f"replicas only ({world} independent GPU replica"
+                                  f"{'s' if world > 1 else ''}, no collective on the data path)",
                    "l2": f"inputs rotate over {head['input_sets']} independent sets "
                          f"(> 2x L2 per rotation)",
                    "timing": "CUDA graph of `steps` calls, CUDA events on its stream"},
@@ -354,12 +400,13 @@ def run_ours(args):
                      "note": f"peak = {pk['source']} HBM copy; achieved = algorithmic bytes "
                              f"({head['bytes_per_step']} per call) / call duration"},
         "e2e": e2e,
-        "gpu_launches": head["gpu_launches"],
+        "gpu_launches": head["gpu_launches"] * world,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "workloads": extra,
     }
     print(json.dumps(line))
+    barrier()
 
 
 def run_reference(args):
@@ -405,17 +452,24 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank, world, local = dist_env()
     if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks exit at once
         if rank == 0:
             run_reference(args)
         return
     if world > 1:
-        # replicas only: each rank runs its own GPU; rank 0 reports
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-    if rank == 0:
+        # replicas only: one independent replica per GPU; the process group
+        # carries the timing barrier and the max-over-ranks reduction only
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
         run_ours(args)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":

@@ -58,7 +58,7 @@ typedef enum { SA_BF16 = 0, SA_F32 = 1 } sa_dtype;
 
 #define SA_HEADS 64
 #define SA_HEAD_DIM 512
-#define SA_MAX_K 2048
+#define SA_MAX_K 1024
 
 /*
  * Bytes of workspace `sa_sparse_attn` needs for this shape on the current

@@ -21,7 +21,7 @@ from ._build import LIB as _LIB_PATH, build  # noqa: F401
 __all__ = ["sparse_attn", "sparse_attn_rope_wo_a", "rope_table", "workspace_size",
            "fused_workspace_size", "check_errors", "SAError", "library", "build"]
 
-HEADS, HEAD_DIM, MAX_K = 64, 512, 2048
+HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
 _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_WORKSPACE",
            4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA"}
 EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn",

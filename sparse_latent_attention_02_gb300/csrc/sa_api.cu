@@ -47,6 +47,12 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const f
     const uint64_t rows = (uint64_t)B * T * SA_HEADS;
     if (!encode_tmap_2d(&p.tm_q, q, rows, SA_HEAD_DIM, 64, 64))
         return SA_ERR_CUDA;
+    // kv rows for four-row gathers (box one row high); with N == 0 nothing is
+    // gathered and the map is left empty
+    if (N > 0 && !encode_tmap_2d(&p.tm_kv, kv, (uint64_t)B * N, SA_HEAD_DIM, 64, 1))
+        return SA_ERR_CUDA;
+    // warm L2 with upcoming rows only when kv cannot stay resident in it
+    p.prefetch_rows = (uint64_t)B * N * SA_HEAD_DIM * 2 > ((uint64_t)96 << 20) ? 1 : 0;
     p.kv = static_cast<const uint16_t *>(kv);
     p.idx = idx;
     p.sink = sink;

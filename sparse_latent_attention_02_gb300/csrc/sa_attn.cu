@@ -16,11 +16,17 @@
 //     The chunk sits in shared memory once, 128-byte swizzled; it is the
 //     K-major A operand of the first product and the MN-major A operand of
 //     the second.  Q (64 KB) stays resident for the whole segment.
-//   * Warp roles: warps 0-3 softmax + epilogue (thread i owns TMEM lane i =
-//     chunk row i during the softmax, output feature 128*tile + i in the
-//     epilogue); warp 4 compacts the index list and gathers rows with 16-byte
-//     cp.async into the swizzled layout; warp 5 allocates TMEM and issues the
-//     MMAs (one elected lane).
+//   * Warp roles (24 warps): warps 0-3 softmax + epilogue (thread i owns
+//     TMEM lane i = chunk row i during the softmax, output feature
+//     128*tile + i in the epilogue); warps 4-19 gather the rows with 16-byte
+//     cp.async straight into the swizzled layout (an SM needs about sixteen
+//     warps of outstanding copies to draw ~40 B/clk of scattered rows from
+//     L2; a single TMA-issuing thread or warp reaches ~6 B/clk); warp 20
+//     compacts each index list into a double-buffered shared list, loads Q
+//     by TMA and, when kv is larger than L2, warms L2 with the next
+//     segment's rows; warp 21 allocates TMEM and issues the MMAs (one
+//     elected lane).  setmaxnreg gives the softmax warpgroup 240 registers
+//     per thread and every other warp 48.
 //   * Online softmax in base 2 with the sink as the starting maximum and a
 //     lazy rescale: the running maximum moves only when a score exceeds it by
 //     more than 2^8, so O^T in TMEM is almost never rewritten.  Row sums are
@@ -37,8 +43,11 @@ namespace sa {
 namespace attn {
 
 constexpr int H = 64, D = 512, CH = 128;
-constexpr int THREADS = 192;
-constexpr int WARP_PRODUCER = 4, WARP_MMA = 5;
+constexpr int NUM_GATHER_WARPS = 16;
+constexpr int WARP_GATHER0 = 4;                 // warps 4 .. 19
+constexpr int WARP_CONTROL = 20, WARP_MMA = 21; // warps 22, 23 only lend registers
+constexpr int THREADS = 24 * 32;
+constexpr int ROWS_PER_GATHER_WARP = CH / NUM_GATHER_WARPS;   // 8
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
 
@@ -51,11 +60,12 @@ constexpr uint32_t P_BYTES = CH * H * 2;        // 16 KB
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_KV = OFF_Q + Q_BYTES;
 constexpr uint32_t OFF_P = OFF_KV + KV_BYTES;
-constexpr uint32_t OFF_IDX = OFF_P + P_BYTES;
-constexpr uint32_t OFF_RED = OFF_IDX + 4 * SA_MAX_K;   // float [4][64]
+constexpr uint32_t OFF_IDX = OFF_P + P_BYTES;          // int32 [2][SA_MAX_K] compacted lists
+constexpr uint32_t OFF_RED = OFF_IDX + 2 * 4 * SA_MAX_K;   // float [4][64]
 constexpr uint32_t OFF_M = OFF_RED + 4 * 64 * 4;       // float [64] running max (log2 units)
 constexpr uint32_t OFF_AUX = OFF_M + 64 * 4;           // float [64] factors / 1/den
-constexpr uint32_t OFF_BAR = OFF_AUX + 64 * 4;         // mbarriers
+constexpr uint32_t OFF_SEGN = OFF_AUX + 64 * 4;        // int [2] list lengths
+constexpr uint32_t OFF_BAR = OFF_SEGN + 16;            // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;        // [0] TMEM base, [1] abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack for 1024-byte alignment
@@ -70,9 +80,12 @@ enum : uint32_t {
     B_PFULL,
     B_PVDONE,
     B_OFREE,
-    B_DONE,
+    B_LFULL0,
+    B_LEMPTY0 = B_LFULL0 + 2,
+    B_DONE = B_LEMPTY0 + 2,
     NUM_BARS
 };
+constexpr uint32_t LEMPTY_ARRIVALS = NUM_GATHER_WARPS + 1 + 4;   // gather warps, MMA, softmax warps
 static_assert(NUM_BARS <= 32, "barrier area");
 
 constexpr uint32_t TMEM_COLS = 512, TM_S = 0, TM_O = 256;
@@ -129,16 +142,49 @@ __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &
     return true;
 }
 
-// Number of entries of idx[q, j0:j1] inside [0, N) (whole warp).
-__device__ __forceinline__ int count_valid(const int32_t *il, int j0, int j1, int N, int lane)
+// Keep the entries of idx[q, j0:j1] that are inside [0, N), in list order, in
+// cidx; `bad` is set if an entry other than -1 falls outside [0, N).
+__device__ __forceinline__ int compact_list(const int32_t *il, int j0, int j1, int N, int32_t *cidx,
+                                            int lane, bool &bad)
 {
     int n = 0;
-    for (int j = j0; j < j1; j += 32) {
-        const int jj = j + lane;
-        const int v = jj < j1 ? __ldg(il + jj) : -1;
-        n += __popc(__ballot_sync(0xffffffffu, v >= 0 && v < N));
+    for (int j = j0; j < j1; j += 256) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int jj = j + 32 * u + lane;
+            v[u] = jj < j1 ? __ldg(il + jj) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool valid = v[u] >= 0 && v[u] < N;
+            bad |= v[u] < -1 || v[u] >= N;
+            const uint32_t m = __ballot_sync(0xffffffffu, valid);
+            if (valid)
+                cidx[n + __popc(m & ((1u << lane) - 1u))] = v[u];
+            n += __popc(m);
+        }
     }
     return n;
+}
+
+// Warm L2 with the latent rows a segment will gather (whole warp).
+__device__ __forceinline__ void prefetch_segment_rows(const AttnParams &p, const Seg &s, int lane)
+{
+    const int32_t *il = p.idx + s.q * (int64_t)p.K;
+    const uint16_t *kvb = p.kv + (size_t)(s.q / p.T) * (size_t)p.N * D;
+    for (int j = s.j0; j < s.j1; j += 256) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int jj = j + 32 * u + lane;
+            v[u] = jj < s.j1 ? __ldg(il + jj) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (v[u] >= 0 && v[u] < p.N)
+                prefetch_l2(kvb + (size_t)v[u] * D, D * 2);
+    }
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
@@ -191,107 +237,160 @@ __device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane, int &hea
 
 // ------------------------------------------------------------------ roles
 
-__device__ void producer_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int lane,
-                              volatile int *abort_flag)
+// Warp 20: compacts every segment's index list (double-buffered), publishes
+// its length, and loads the segment's Q by TMA.
+__device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int lane,
+                             volatile int *abort_flag)
 {
-    int32_t *cidx = reinterpret_cast<int32_t *>(smem + OFF_IDX);
+    int *segn = reinterpret_cast<int *>(smem + OFF_SEGN);
     const uint32_t bar0 = sbase + OFF_BAR;
-    uint32_t ph_qempty = 0, ph_kvfree[4] = {0, 0, 0, 0};
+    uint32_t ph_qempty = 0, ph_lempty[2] = {0, 0};
     uint32_t q_loads = 0;
     bool ok = true;
     SegIter it;
     seg_begin(p, it);
     Seg s;
-    while (ok && seg_next(p, it, s)) {
-        const int32_t *il = p.idx + s.q * (int64_t)p.K;
-        // compact the valid entries of this segment into shared memory
-        int n = 0;
-        bool bad = false;
-        for (int j = s.j0; j < s.j1; j += 32) {
-            const int jj = j + lane;
-            const int v = jj < s.j1 ? __ldg(il + jj) : -1;
-            const bool valid = v >= 0 && v < p.N;
-            bad |= (jj < s.j1) && (v < -1 || v >= p.N);
-            const uint32_t m = __ballot_sync(0xffffffffu, valid);
-            if (valid)
-                cidx[n + __popc(m & ((1u << lane) - 1u))] = v;
-            n += __popc(m);
-        }
-        if (__any_sync(0xffffffffu, bad) && lane == 0)
-            atomicOr(p.err, ERRBIT_INDEX);
-        __syncwarp();
-        const int nc = (n + CH - 1) / CH;
-        if (nc == 0)
-            continue;
-
-        // Q of this query: wait until the previous segment's QK products are done with it
-        ok = warp_wait(bar0 + 8 * B_QEMPTY, ph_qempty ^ 1u, abort_flag, p.timeout_ns, lane);
-        ph_qempty ^= 1u;
+    bool have = seg_next(p, it, s);
+    if (have && p.prefetch_rows)
+        prefetch_segment_rows(p, s, lane);
+    for (int k = 0; ok && have; ++k) {
+        const int b = k & 1;
+        // every consumer of this list buffer is done with the segment before
+        ok = warp_wait(bar0 + 8 * (B_LEMPTY0 + b), ph_lempty[b] ^ 1u, abort_flag, p.timeout_ns, lane);
+        ph_lempty[b] ^= 1u;
         if (!ok)
             break;
-        if (lane == 0) {
-            const uint32_t bq = bar0 + 8 * B_QFULL;
-            mbar_arrive_expect_tx(bq, Q_BYTES);
-            for (int kb = 0; kb < 8; ++kb)
-                tma_load_2d(sbase + OFF_Q + kb * QBLK_BYTES, &p.tm_q, kb * 64, (int32_t)(s.q * H), bq);
+        int32_t *cidx = reinterpret_cast<int32_t *>(smem + OFF_IDX) + b * SA_MAX_K;
+        bool bad = false;
+        const int n = compact_list(p.idx + s.q * (int64_t)p.K, s.j0, s.j1, p.N, cidx, lane, bad);
+        if (__any_sync(0xffffffffu, bad) && lane == 0)
+            atomicOr(p.err, ERRBIT_INDEX);
+        if (lane == 0)
+            segn[b] = n;
+        __syncwarp();
+        mbar_arrive(bar0 + 8 * (B_LFULL0 + b));   // all 32 lanes: each releases its entries
+        if (p.prefetch_rows) {
+            SegIter la = it;
+            Seg sn;
+            if (seg_next(p, la, sn))
+                prefetch_segment_rows(p, sn, lane);
         }
-        ++q_loads;
+        if (n > 0) {
+            // Q of this query, once the previous segment's QK products are done with it
+            ok = warp_wait(bar0 + 8 * B_QEMPTY, ph_qempty ^ 1u, abort_flag, p.timeout_ns, lane);
+            ph_qempty ^= 1u;
+            if (!ok)
+                break;
+            if (lane == 0) {
+                const uint32_t bq = bar0 + 8 * B_QFULL;
+                mbar_arrive_expect_tx(bq, Q_BYTES);
+                for (int kb = 0; kb < 8; ++kb)
+                    tma_load_2d(sbase + OFF_Q + kb * QBLK_BYTES, &p.tm_q, kb * 64, (int32_t)(s.q * H), bq);
+            }
+            ++q_loads;
+        }
+        have = seg_next(p, it, s);
+    }
+    // a Q load still in flight must land before the CTA can exit
+    if (lane == 0 && q_loads > 0)
+        drain_wait(bar0 + 8 * B_QFULL, (q_loads - 1u) & 1u, p.timeout_ns);
+    __syncwarp();
+}
 
+// Warps 4-19: gather the compacted rows, chunk by chunk, tile by tile (two
+// 64-feature slices of the 128 rows per tile).  Warp gi copies rows
+// 8gi .. 8gi+7; rows past the end of the list are zero-filled.
+__device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int gi, int lane,
+                            volatile int *abort_flag)
+{
+    const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
+    const uint32_t bar0 = sbase + OFF_BAR;
+    uint32_t ph_lfull[2] = {0, 0}, ph_kvfree[4] = {0, 0, 0, 0};
+    bool ok = true;
+    SegIter it;
+    seg_begin(p, it);
+    Seg s;
+    for (int k = 0; ok && seg_next(p, it, s); ++k) {
+        const int b = k & 1;
+        ok = warp_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns, lane);
+        ph_lfull[b] ^= 1u;
+        if (!ok)
+            break;
+        const int n = segn[b];
+        const int32_t *cidx = reinterpret_cast<const int32_t *>(smem + OFF_IDX) + b * SA_MAX_K;
+        const int nc = (n + CH - 1) / CH;
         const uint16_t *kvb = p.kv + (size_t)(s.q / p.T) * (size_t)p.N * D;
-        const int half = lane >> 4, within = lane & 15;
         for (int c = 0; c < nc && ok; ++c) {
             const int rows = min(CH, n - c * CH);
-            const int32_t *crow = cidx + c * CH;
+            // this lane's four (row, 16-byte piece) jobs; the rows are the same for every tile
+            int r[4], row[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                r[i] = ROWS_PER_GATHER_WARP * gi + ((i * 32 + lane) >> 4);
+                row[i] = r[i] < rows ? cidx[c * CH + r[i]] : -1;
+            }
+            const int pc = lane & 15;   // piece: slice (2d + pc / 8), 16-byte chunk pc % 8
             for (int d = 0; d < 4; ++d) {
                 ok = warp_wait(bar0 + 8 * (B_KVFREE0 + d), ph_kvfree[d] ^ 1u, abort_flag, p.timeout_ns,
                                lane);
                 ph_kvfree[d] ^= 1u;
                 if (!ok)
                     break;
-                // slices 2d, 2d+1: 128 rows x 2 x 128 B = 2048 pieces of 16 B, 64 per lane
-                const int sl = 2 * d + (within >> 3), pc = within & 7;
-                const uint32_t dst0 = sbase + OFF_KV + sl * SLICE_BYTES;
-                const uint16_t *src0 = kvb + sl * 64 + pc * 8;
-#pragma unroll 8
-                for (int i = 0; i < 64; ++i) {
-                    const int r = 2 * i + half;
-                    const bool v = r < rows;
-                    const int row = v ? crow[r] : 0;
-                    cp_async16(dst0 + r * 128 + ((pc ^ (r & 7)) << 4), src0 + (size_t)row * D,
-                               v ? 16u : 0u);
+                const int sl = 2 * d + (pc >> 3), ch = pc & 7;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r[i] * 128 + ((ch ^ (r[i] & 7)) << 4);
+                    const uint16_t *src = kvb + (size_t)(row[i] < 0 ? 0 : row[i]) * D + sl * 64 + ch * 8;
+                    cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
                 }
                 cp_async_commit();
                 if (d > 0) {
                     cp_async_wait<1>();
                     fence_proxy_async_smem();
-                    mbar_arrive(bar0 + 8 * (B_KVFULL0 + d - 1));
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar0 + 8 * (B_KVFULL0 + d - 1));
                 }
             }
             if (!ok)
                 break;
             cp_async_wait<0>();
             fence_proxy_async_smem();
-            mbar_arrive(bar0 + 8 * (B_KVFULL0 + 3));
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar0 + 8 * (B_KVFULL0 + 3));
         }
+        if (!ok)
+            break;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar0 + 8 * (B_LEMPTY0 + b));
     }
     cp_async_wait_all();
-    // a Q load still in flight must land before the CTA can exit
-    if (q_loads > 0 && lane == 0)
-        drain_wait(bar0 + 8 * B_QFULL, (q_loads - 1u) & 1u, p.timeout_ns);
     __syncwarp();
 }
 
-__device__ void mma_role(const AttnParams &p, uint32_t sbase, uint32_t tmem, int lane,
+__device__ void mma_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tmem, int lane,
                          volatile int *abort_flag)
 {
     const uint32_t bar0 = sbase + OFF_BAR;
+    const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
     uint32_t ph_qfull = 0, ph_kvfull[4] = {0, 0, 0, 0}, ph_pfull = 0, ph_ofree = 0;
+    uint32_t ph_lfull[2] = {0, 0};
     bool ok = true;
     SegIter it;
     seg_begin(p, it);
     Seg s;
-    while (ok && seg_next(p, it, s)) {
-        const int n = count_valid(p.idx + s.q * (int64_t)p.K, s.j0, s.j1, p.N, lane);
+    for (int k = 0; ok && seg_next(p, it, s); ++k) {
+        const int b = k & 1;
+        ok = warp_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns, lane);
+        ph_lfull[b] ^= 1u;
+        if (!ok)
+            break;
+        const int n = segn[b];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar0 + 8 * (B_LEMPTY0 + b));
         const int nc = (n + CH - 1) / CH;
         if (nc == 0)
             continue;
@@ -376,15 +475,24 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     float *aux = reinterpret_cast<float *>(smem + OFF_AUX);
     const uint32_t bar0 = sbase + OFF_BAR;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's TMEM lane quarter
-    uint32_t ph_sfull = 0, ph_pvdone = 0;
+    const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
+    uint32_t ph_sfull = 0, ph_pvdone = 0, ph_lfull[2] = {0, 0};
     SegIter it;
     seg_begin(p, it);
     Seg s;
-    while (seg_next(p, it, s)) {
-        const int n = count_valid(p.idx + s.q * (int64_t)p.K, s.j0, s.j1, p.N, lane);
+    for (int k = 0; seg_next(p, it, s); ++k) {
+        const int b = k & 1;
+        const bool w0 = warp_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns, lane);
+        ph_lfull[b] ^= 1u;
+        // also: the previous epilogue is done with m_s / aux
+        if (bar_red_or(1, 128, !w0 || *abort_flag))
+            break;
+        const int n = segn[b];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar0 + 8 * (B_LEMPTY0 + b));
         const int nc = (n + CH - 1) / CH;
 
-        bar_sync(1, 128);   // the previous epilogue is done with m_s / aux
         if (t < 64)
             m_s[t] = __ldg(p.sink + t) * LOG2E;
         bar_sync(1, 128);
@@ -561,10 +669,23 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 for (int h = 0; h < 64; ++h)
                     po[h * 512] = o[h];
             } else {
-                __nv_bfloat16 *po = reinterpret_cast<__nv_bfloat16 *>(p.out) + (size_t)s.q * (H * D) + dim;
+                // stage the tile as [64 heads][128 features] bf16 in the P buffer
+                // (free once the last PV is done), then write whole 256-byte head
+                // rows with 16-byte stores
+                uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
 #pragma unroll
                 for (int h = 0; h < 64; ++h)
-                    po[h * 512] = __float2bfloat16_rn(o[h]);
+                    stg[h * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h]));
+                bar_sync(1, 128);
+                uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = t + 128 * i;   // 16-byte piece c: head c / 16, part c % 16
+                    const int h = c >> 4, part = c & 15;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
+                    *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
+                }
+                bar_sync(1, 128);
             }
         }
         if (nc > 0) {
@@ -589,13 +710,17 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         mbar_init(bar0 + 8 * B_QFULL, 1);
         mbar_init(bar0 + 8 * B_QEMPTY, 1);
         for (int d = 0; d < 4; ++d) {
-            mbar_init(bar0 + 8 * (B_KVFULL0 + d), 32);
+            mbar_init(bar0 + 8 * (B_KVFULL0 + d), NUM_GATHER_WARPS);
             mbar_init(bar0 + 8 * (B_KVFREE0 + d), 1);
         }
         mbar_init(bar0 + 8 * B_SFULL, 1);
         mbar_init(bar0 + 8 * B_PFULL, 128);
         mbar_init(bar0 + 8 * B_PVDONE, 1);
         mbar_init(bar0 + 8 * B_OFREE, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar0 + 8 * (B_LFULL0 + b), 32);
+            mbar_init(bar0 + 8 * (B_LEMPTY0 + b), LEMPTY_ARRIVALS);
+        }
         mbar_init(bar0 + 8 * B_DONE, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -610,12 +735,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == WARP_PRODUCER)
-        producer_role(p, smem, sbase, lane, abort_flag);
-    else if (warp == WARP_MMA)
-        mma_role(p, sbase, tmem, lane, abort_flag);
-    else
+    if (warp < 4) {
+        // the softmax warpgroup keeps 64 scores and 64 row sums per thread
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 240;" ::: "memory");
         softmax_role(p, smem, sbase, tmem, warp, lane, abort_flag);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
+        if (warp < WARP_GATHER0 + NUM_GATHER_WARPS)
+            gather_role(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
+        else if (warp == WARP_CONTROL)
+            control_role(p, smem, sbase, lane, abort_flag);
+        else if (warp == WARP_MMA)
+            mma_role(p, smem, sbase, tmem, lane, abort_flag);
+    }
 
     tc_fence_before();
     __syncthreads();
@@ -634,13 +766,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 //   M = max(sink*log2e, max_s m_s);  w_s = 2^(m_s - M)
 //   o = sum_s w_s O_s / (sum_s w_s l_s + 2^(sink*log2e - M))
 constexpr int MAX_PIECES = SA_MAX_K / 128 + 2;
+constexpr int COMBINE_HEADS = 4;   // heads per block: grid (B*T, 64 / COMBINE_HEADS)
 
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p)
 {
-    __shared__ float w_s[MAX_PIECES][64];
-    __shared__ float inv_den[64];
+    __shared__ float w_s[MAX_PIECES][COMBINE_HEADS];
+    __shared__ float inv_den[COMBINE_HEADS];
     __shared__ int slots[MAX_PIECES];
     const int64_t q = blockIdx.x;
+    const int h0 = blockIdx.y * COMBINE_HEADS;
     const int64_t e0 = q * p.K, e1 = e0 + p.K;
     const int c0 = (int)(e0 / p.per_cta), c1 = (int)((e1 - 1) / p.per_cta);
     if (c0 == c1)
@@ -652,53 +786,59 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
         slots[t] = ((int64_t)c * p.per_cta >= e0) ? 2 * c : 2 * c + 1;
     }
     __syncthreads();
-    if (t < 64) {
-        const float sl = __ldg(p.sink + t) * LOG2E;
+    if (t < COMBINE_HEADS) {
+        const int h = h0 + t;
+        const float sl = __ldg(p.sink + h) * LOG2E;
         float M = sl;
         for (int i = 0; i < np; ++i)
-            M = fmaxf(M, p.part[(size_t)slots[i] * PART_STRIDE + PART_O + t]);
+            M = fmaxf(M, p.part[(size_t)slots[i] * PART_STRIDE + PART_O + h]);
         float den = 0.f, lsum = 0.f;
         for (int i = 0; i < np; ++i) {
             const float *pm = p.part + (size_t)slots[i] * PART_STRIDE + PART_O;
-            const float w = (M == -INFINITY) ? 0.f : ex2(pm[t] - M);
+            const float w = (M == -INFINITY) ? 0.f : ex2(pm[h] - M);
             w_s[i][t] = w;
-            den += w * pm[64 + t];
-            lsum += pm[64 + t];
+            den += w * pm[64 + h];
+            lsum += pm[64 + h];
         }
         den += (M == -INFINITY) ? 0.f : ex2(sl - M);
         inv_den[t] = (lsum > 0.f && den > 0.f) ? 1.f / den : 0.f;
     }
     __syncthreads();
-    // 64 x 512 outputs, 4 consecutive features per thread per step
-    for (int e = 4 * t; e < H * D; e += 4 * 256) {
-        const int h = e >> 9, dim = e & 511;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int i = 0; i < np; ++i) {
-            const float4 v = *reinterpret_cast<const float4 *>(p.part + (size_t)slots[i] * PART_STRIDE + e);
-            const float w = w_s[i][h];
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-        }
-        float o[4] = {acc.x * inv_den[h], acc.y * inv_den[h], acc.z * inv_den[h], acc.w * inv_den[h]};
-        if (p.rope_dim > 0 && dim >= D - p.rope_dim) {
-            const float *cs = p.rope + ((size_t)(q % p.T) * (p.rope_dim >> 1) + ((dim - (D - p.rope_dim)) >> 1)) * 2;
+    // this block's 4 heads x 512 features: 8 consecutive features per thread
+    const int hl = (8 * t) >> 9;
+    const int dim = (8 * t) & 511;
+    const int e = (h0 + hl) * D + dim;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.part + (size_t)slots[i] * PART_STRIDE + e);
+        const float4 a = src[0], b = src[1];
+        const float w = w_s[i][hl];
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+    }
+    float o[8];
 #pragma unroll
-            for (int k = 0; k < 4; k += 2) {
-                const float c = __ldg(cs + k), sn = __ldg(cs + k + 1);
-                const float a = o[k], b = o[k + 1];
-                o[k] = a * c + b * sn;
-                o[k + 1] = -a * sn + b * c;
-            }
+    for (int k = 0; k < 8; ++k)
+        o[k] = acc[k] * inv_den[hl];
+    if (p.rope_dim > 0 && dim >= D - p.rope_dim) {
+        const float *cs = p.rope + ((size_t)(q % p.T) * (p.rope_dim >> 1) + ((dim - (D - p.rope_dim)) >> 1)) * 2;
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const float c = __ldg(cs + k), sn = __ldg(cs + k + 1);
+            const float a = o[k], b = o[k + 1];
+            o[k] = a * c + b * sn;
+            o[k + 1] = -a * sn + b * c;
         }
-        if (p.out_f32) {
-            *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + q * (H * D) + e) =
-                make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-            uint2 pk = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
-            *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.out) + q * (H * D) + e) = pk;
-        }
+    }
+    if (p.out_f32) {
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + q * (H * D) + e);
+        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    } else {
+        *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) + q * (H * D) + e) =
+            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                       pack_bf16x2(o[6], o[7]));
     }
 }
 
@@ -739,14 +879,10 @@ size_t attn_workspace_bytes(int64_t BT, int K, int num_sms)
 
 cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
 {
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(attn::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn::SMEM_BYTES);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
+    cudaError_t ea = cudaFuncSetAttribute(attn::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)attn::SMEM_BYTES);
+    if (ea != cudaSuccess)
+        return ea;
     p.split = s.split;
     p.per_cta = s.per_cta;
     if (s.grid == 0)
@@ -755,7 +891,7 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || !s.split)
         return e;
-    attn::combine_kernel<<<(unsigned)p.BT, 256, 0, st>>>(p);
+    attn::combine_kernel<<<dim3((unsigned)p.BT, attn::H / attn::COMBINE_HEADS), 256, 0, st>>>(p);
     return cudaGetLastError();
 }
 

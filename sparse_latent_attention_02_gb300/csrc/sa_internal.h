@@ -21,6 +21,7 @@ constexpr int PART_STRIDE = PART_O + 128;
 
 struct AttnParams {
     CUtensorMap tm_q;          // q as 2-D [B*T*H rows, D cols] bf16, box 64x64, 128B swizzle
+    CUtensorMap tm_kv;         // kv as 2-D [B*N rows, D cols] bf16, box 64x1 (row gathers), 128B swizzle
     const uint16_t *kv;        // bf16 [B, N, D]
     const int32_t *idx;        // int32 [B*T, K]
     const float *sink;         // fp32 [H]
@@ -35,6 +36,7 @@ struct AttnParams {
     int split;                 // 0: whole queries, CTA i takes i, i+grid, ...; 1: entry ranges
     int64_t per_cta;           // split: raw list entries per CTA
     int rope_dim;              // 0 = no rotary epilogue
+    int prefetch_rows;         // 1: warm L2 with the next segment's rows (kv larger than L2)
     uint64_t timeout_ns;       // bound on every device-side wait
 };
 

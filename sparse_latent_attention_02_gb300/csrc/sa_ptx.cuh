@@ -57,6 +57,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that lets the thread sleep (up to `hint_ns`) until the phase
+// completes, instead of returning at once: waiting warps then stop competing
+// for issue slots with the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Poll an mbarrier phase until it completes, the CTA-wide abort flag is set,
 // or `limit_ns` of wall time passes.  Returns true when the phase completed.
 // On a timeout the caller's abort flag is raised so that every other role of
@@ -66,17 +82,15 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity))
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 200000u))
             return true;
-        if ((i & 63u) == 0) {
-            if (*abort_flag)
-                return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
-                *abort_flag = 1;
-                return false;
-            }
+        if (*abort_flag)
+            return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            return false;
         }
     }
 }
@@ -143,6 +157,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Four-row gather: rows y0..y3, columns [x, x + box) of a 2-D tensor map whose
+// box is one row high, into four consecutive box rows at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int32_t x, int32_t y0,
+                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
         : "memory");
 }
 
