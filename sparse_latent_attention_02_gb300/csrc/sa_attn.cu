@@ -370,100 +370,95 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
     __syncwarp();
 }
 
-__device__ void mma_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tmem, int lane,
+// Lane 0 of warp 21 runs this role alone: the tensor pipe reaches its rate
+// only when MMAs are issued back to back, so the issuing thread avoids warp
+// divergence and keeps its descriptor arithmetic to one add per MMA (the
+// start-address field, address >> 4, is the low 14 bits of a descriptor).
+__device__ void mma_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tmem,
                          volatile int *abort_flag)
 {
     const uint32_t bar0 = sbase + OFF_BAR;
     const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
     uint32_t ph_qfull = 0, ph_kvfull[4] = {0, 0, 0, 0}, ph_pfull = 0, ph_ofree = 0;
     uint32_t ph_lfull[2] = {0, 0};
+    // S^T = K . Q^T: A = chunk (K-major), B = Q (K-major)
+    const uint64_t d_qk_a = smem_desc_sw128(sbase + OFF_KV, 16, 1024);
+    const uint64_t d_qk_b = smem_desc_sw128(sbase + OFF_Q, 16, 1024);
+    // O^T += V^T . P^T: A = chunk (MN-major, 64-feature groups one slice apart), B = P^T (MN-major)
+    const uint64_t d_pv_a = smem_desc_sw128(sbase + OFF_KV, SLICE_BYTES, 1024);
+    const uint64_t d_pv_b = smem_desc_sw128(sbase + OFF_P, 8192, 1024);
     bool ok = true;
     SegIter it;
     seg_begin(p, it);
     Seg s;
     for (int k = 0; ok && seg_next(p, it, s); ++k) {
         const int b = k & 1;
-        ok = warp_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns, lane);
+        ok = bounded_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns);
         ph_lfull[b] ^= 1u;
         if (!ok)
             break;
         const int n = segn[b];
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(bar0 + 8 * (B_LEMPTY0 + b));
+        mbar_arrive(bar0 + 8 * (B_LEMPTY0 + b));
         const int nc = (n + CH - 1) / CH;
         if (nc == 0)
             continue;
-        ok = warp_wait(bar0 + 8 * B_QFULL, ph_qfull, abort_flag, p.timeout_ns, lane);
+        ok = bounded_wait(bar0 + 8 * B_QFULL, ph_qfull, abort_flag, p.timeout_ns);
         ph_qfull ^= 1u;
         if (!ok)
             break;
         for (int c = 0; c < nc && ok; ++c) {
-            // S^T = K_chunk . Q^T over 32 steps of 16 features
+            // S^T = K_chunk . Q^T over 32 steps of 16 features, tile by tile as they land
+#pragma unroll
             for (int d = 0; d < 4; ++d) {
-                ok = warp_wait(bar0 + 8 * (B_KVFULL0 + d), ph_kvfull[d], abort_flag, p.timeout_ns, lane);
+                ok = bounded_wait(bar0 + 8 * (B_KVFULL0 + d), ph_kvfull[d], abort_flag, p.timeout_ns);
                 ph_kvfull[d] ^= 1u;
                 if (!ok)
                     break;
                 tc_fence_after();
-                if (lane == 0) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int kk = 8 * d + k, sl = kk >> 2, sub = kk & 3;
-                        const uint64_t a =
-                            smem_desc_sw128(sbase + OFF_KV + sl * SLICE_BYTES + sub * 32, 16, 1024);
-                        const uint64_t b =
-                            smem_desc_sw128(sbase + OFF_Q + sl * QBLK_BYTES + sub * 32, 16, 1024);
-                        mma_bf16_ss(tmem + TM_S, a, b, IDESC_QK, kk > 0 ? 1u : 0u);
-                    }
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const int kk = 8 * d + k8;
+                    const uint32_t oa = ((kk >> 2) * SLICE_BYTES + (kk & 3) * 32) >> 4;
+                    const uint32_t ob = ((kk >> 2) * QBLK_BYTES + (kk & 3) * 32) >> 4;
+                    mma_bf16_ss(tmem + TM_S, d_qk_a + oa, d_qk_b + ob, IDESC_QK, kk > 0 ? 1u : 0u);
                 }
-                __syncwarp();
             }
             if (!ok)
                 break;
-            if (lane == 0) {
-                mma_commit(bar0 + 8 * B_SFULL);
-                if (c == nc - 1)
-                    mma_commit(bar0 + 8 * B_QEMPTY);
-            }
-            __syncwarp();
-            ok = warp_wait(bar0 + 8 * B_PFULL, ph_pfull, abort_flag, p.timeout_ns, lane);
+            mma_commit(bar0 + 8 * B_SFULL);
+            if (c == nc - 1)
+                mma_commit(bar0 + 8 * B_QEMPTY);
+            ok = bounded_wait(bar0 + 8 * B_PFULL, ph_pfull, abort_flag, p.timeout_ns);
             ph_pfull ^= 1u;
             if (!ok)
                 break;
             if (c == 0) {
                 // the previous segment's epilogue must have read O^T out of TMEM
-                ok = warp_wait(bar0 + 8 * B_OFREE, ph_ofree ^ 1u, abort_flag, p.timeout_ns, lane);
+                ok = bounded_wait(bar0 + 8 * B_OFREE, ph_ofree ^ 1u, abort_flag, p.timeout_ns);
                 ph_ofree ^= 1u;
                 if (!ok)
                     break;
             }
             tc_fence_after();
             // O^T += V^T . P^T: four 128-feature tiles, 8 steps of 16 rows each
-            if (lane == 0) {
+            const uint32_t acc0 = c > 0 ? 1u : 0u;
 #pragma unroll
-                for (int d = 0; d < 4; ++d) {
+            for (int d = 0; d < 4; ++d) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = smem_desc_sw128(
-                            sbase + OFF_KV + (2 * d) * SLICE_BYTES + kk * 2048, SLICE_BYTES, 1024);
-                        const uint64_t b = smem_desc_sw128(sbase + OFF_P + kk * 2048, 8192, 1024);
-                        mma_bf16_ss(tmem + TM_O + 64 * d, a, b, IDESC_PV,
-                                    (c > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar0 + 8 * (B_KVFREE0 + d));
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t oa = ((2 * d) * SLICE_BYTES + kk * 2048) >> 4;
+                    const uint32_t ob = (kk * 2048) >> 4;
+                    mma_bf16_ss(tmem + TM_O + 64 * d, d_pv_a + oa, d_pv_b + ob, IDESC_PV,
+                                kk > 0 ? 1u : acc0);
                 }
-                mma_commit(bar0 + 8 * B_PVDONE);
+                mma_commit(bar0 + 8 * (B_KVFREE0 + d));
             }
-            __syncwarp();
+            mma_commit(bar0 + 8 * B_PVDONE);
         }
     }
     // every MMA issued must complete before TMEM is released
-    if (lane == 0) {
-        mma_commit(bar0 + 8 * B_DONE);
-        drain_wait(bar0 + 8 * B_DONE, 0, p.timeout_ns);
-    }
-    __syncwarp();
+    mma_commit(bar0 + 8 * B_DONE);
+    drain_wait(bar0 + 8 * B_DONE, 0, p.timeout_ns);
 }
 
 __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tmem,
@@ -504,11 +499,14 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
 
         bool aborted = false;
         for (int c = 0; c < nc; ++c) {
-            const bool w1 = warp_wait(bar0 + 8 * B_SFULL, ph_sfull, abort_flag, p.timeout_ns, lane);
+            // S^T of this chunk is ready; PV of the previous chunk (issued before
+            // this chunk's QK) has then finished too, so P may be rewritten and
+            // O^T rescaled
+            bool wok = warp_wait(bar0 + 8 * B_SFULL, ph_sfull, abort_flag, p.timeout_ns, lane);
             ph_sfull ^= 1u;
-            if (bar_red_or(1, 128, !w1 || *abort_flag)) {
-                aborted = true;
-                break;
+            if (c > 0) {
+                wok = warp_wait(bar0 + 8 * B_PVDONE, ph_pvdone, abort_flag, p.timeout_ns, lane) && wok;
+                ph_pvdone ^= 1u;
             }
             tc_fence_after();
             uint32_t r[64];
@@ -523,18 +521,13 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 x[h] = vrow ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
                 need |= x[h] > m_s[h] + RESCALE_THRESHOLD;
             }
-            // PV of the previous chunk must be complete before P is rewritten
-            // or O^T rescaled.
-            bool w2 = true;
-            if (c > 0) {
-                w2 = warp_wait(bar0 + 8 * B_PVDONE, ph_pvdone, abort_flag, p.timeout_ns, lane);
-                ph_pvdone ^= 1u;
-            }
-            if (bar_red_or(1, 128, !w2 || *abort_flag)) {
-                aborted = true;
-                break;
-            }
-            if (bar_red_or(1, 128, need)) {
+            // one barrier in the common case: it carries the rescale vote and
+            // any failed wait; a second one tells the two apart
+            if (bar_red_or(1, 128, need || !wok || *abort_flag)) {
+                if (bar_red_or(1, 128, !wok || *abort_flag)) {
+                    aborted = true;
+                    break;
+                }
                 // move the running maximum to this chunk's maximum (per head)
                 int h0;
                 warp_reduce64<true>(x, lane, h0);
@@ -628,64 +621,67 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         }
         bar_sync(1, 128);
 
-        // epilogue: thread t owns feature 128*d + t of every head
+        // epilogue: thread t owns feature 128*d + t of every head; TMEM is read
+        // in halves of 32 heads
         const bool rope_here = s.full && p.rope_dim > 0;
+        uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
 #pragma unroll 1
-        for (int d = 0; d < 4; ++d) {
+        for (int e = 0; e < 8; ++e) {
+            const int d = e >> 1, hh = e & 1;
             const int dim = 128 * d + t;
-            float o[64];
+            uint32_t u[32];
             if (nc > 0) {
-                uint32_t u[64];
-                tmem_ld32(tl + TM_O + 64 * d, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-                tmem_ld32(tl + TM_O + 64 * d + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+                tmem_ld32(tl + TM_O + 32 * e, u);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    o[h] = __uint_as_float(u[h]) * aux[h];
+                for (int i = 0; i < 32; ++i)
+                    u[i] = __float_as_uint(__uint_as_float(u[i]) * aux[32 * hh + i]);
             } else {
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    o[h] = 0.f;
+                for (int i = 0; i < 32; ++i)
+                    u[i] = 0u;
             }
             if (rope_here && dim >= D - p.rope_dim) {   // warp-uniform
-                const int i = (dim - (D - p.rope_dim)) >> 1;
-                const float *cs = p.rope + ((size_t)(s.q % p.T) * (p.rope_dim >> 1) + i) * 2;
+                const int pi = (dim - (D - p.rope_dim)) >> 1;
+                const float *cs = p.rope + ((size_t)(s.q % p.T) * (p.rope_dim >> 1) + pi) * 2;
                 const float cth = __ldg(cs), sth = __ldg(cs + 1);
                 const bool odd = dim & 1;
 #pragma unroll
-                for (int h = 0; h < 64; ++h) {
-                    const float other = __shfl_xor_sync(0xffffffffu, o[h], 1);
-                    o[h] = odd ? (o[h] * cth - other * sth) : (o[h] * cth + other * sth);
+                for (int i = 0; i < 32; ++i) {
+                    const float o = __uint_as_float(u[i]);
+                    const float other = __shfl_xor_sync(0xffffffffu, o, 1);
+                    u[i] = __float_as_uint(odd ? (o * cth - other * sth) : (o * cth + other * sth));
                 }
             }
             if (!s.full) {
-                float *po = p.part + (size_t)s.slot * PART_STRIDE + dim;
+                float *po = p.part + (size_t)s.slot * PART_STRIDE + (size_t)(32 * hh) * 512 + dim;
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    po[h * 512] = o[h];
+                for (int i = 0; i < 32; ++i)
+                    po[i * 512] = __uint_as_float(u[i]);
             } else if (p.out_f32) {
-                float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + dim;
+                float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + (size_t)(32 * hh) * 512 + dim;
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    po[h * 512] = o[h];
+                for (int i = 0; i < 32; ++i)
+                    po[i * 512] = __uint_as_float(u[i]);
             } else {
                 // stage the tile as [64 heads][128 features] bf16 in the P buffer
-                // (free once the last PV is done), then write whole 256-byte head
-                // rows with 16-byte stores
-                uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
+                // (free once the last PV is done); after both halves, write whole
+                // 256-byte head rows with 16-byte stores
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    stg[h * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h]));
-                bar_sync(1, 128);
-                uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
+                for (int i = 0; i < 32; ++i)
+                    stg[(32 * hh + i) * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[i])));
+                if (hh == 1) {
+                    bar_sync(1, 128);
+                    uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = t + 128 * i;   // 16-byte piece c: head c / 16, part c % 16
-                    const int h = c >> 4, part = c & 15;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
-                    *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = t + 128 * i;   // 16-byte piece c: head c / 16, part c % 16
+                        const int h = c >> 4, part = c & 15;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
+                        *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
+                    }
+                    bar_sync(1, 128);
                 }
-                bar_sync(1, 128);
             }
         }
         if (nc > 0) {
@@ -745,8 +741,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             gather_role(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
         else if (warp == WARP_CONTROL)
             control_role(p, smem, sbase, lane, abort_flag);
-        else if (warp == WARP_MMA)
-            mma_role(p, smem, sbase, tmem, lane, abort_flag);
+        else if (warp == WARP_MMA && lane == 0)
+            mma_role(p, smem, sbase, tmem, abort_flag);
     }
 
     tc_fence_before();
