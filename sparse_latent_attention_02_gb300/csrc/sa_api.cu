@@ -66,6 +66,11 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const f
     p.K = K;
     p.out_f32 = out_f32 ? 1 : 0;
     p.timeout_ns = wait_timeout_ns();
+    // Test hook for failure detection: SA_TEST_HOLD_LISTS=1 makes the kernel
+    // withhold its first index list, so its bounded waits run out and the call
+    // reports SA_ERR_TIMEOUT without faulting or hanging the GPU.
+    const char *hold = std::getenv("SA_TEST_HOLD_LISTS");
+    p.hold_lists = (hold && hold[0] == '1') ? 1 : 0;
     return SA_OK;
 }
 

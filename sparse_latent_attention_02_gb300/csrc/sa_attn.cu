@@ -102,20 +102,20 @@ struct Seg {
 };
 
 struct SegIter {
-    int64_t lo, hi, cur, q;
+    int64_t q;
+    bool done;
 };
 
 __device__ __forceinline__ void seg_begin(const AttnParams &p, SegIter &it)
 {
-    if (p.split) {
-        it.lo = (int64_t)blockIdx.x * p.per_cta;
-        it.hi = min(it.lo + p.per_cta, p.BT * (int64_t)p.K);
-        it.cur = it.lo;
-    } else {
-        it.q = blockIdx.x;
-    }
+    (void)p;
+    it.q = blockIdx.x;
+    it.done = false;
 }
 
+// Whole mode: CTA i takes queries i, i + grid, ...  Split mode: CTA c takes
+// piece c % pieces (entries [i*per_cta, min((i+1)*per_cta, K))) of query
+// c / pieces and leaves its partial result in slot c.
 __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &s)
 {
     if (!p.split) {
@@ -129,17 +129,16 @@ __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &
         it.q += gridDim.x;
         return true;
     }
-    if (it.cur >= it.hi)
+    if (it.done)
         return false;
-    s.q = it.cur / p.K;
-    const int64_t qs = s.q * p.K;
-    const int64_t end = min(it.hi, qs + p.K);
-    s.j0 = (int)(it.cur - qs);
-    s.j1 = (int)(end - qs);
-    s.full = (s.j0 == 0 && s.j1 == p.K);
-    s.slot = (it.cur == it.lo) ? 2 * (int)blockIdx.x : 2 * (int)blockIdx.x + 1;
-    it.cur = end;
-    return true;
+    it.done = true;
+    const int piece = (int)(blockIdx.x % (unsigned)p.pieces);
+    s.q = blockIdx.x / p.pieces;
+    s.j0 = (int)(piece * p.per_cta);
+    s.j1 = (int)min((int64_t)p.K, (piece + 1) * p.per_cta);
+    s.full = false;
+    s.slot = (int)blockIdx.x;
+    return s.q < p.BT && s.j0 < s.j1;
 }
 
 // Keep the entries of idx[q, j0:j1] that are inside [0, N), in list order, in
@@ -268,7 +267,11 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         if (lane == 0)
             segn[b] = n;
         __syncwarp();
-        mbar_arrive(bar0 + 8 * (B_LFULL0 + b));   // all 32 lanes: each releases its entries
+        // all 32 lanes arrive: each releases its entries.  The failure-detection
+        // test withholds the first list so that every consumer's bounded wait
+        // runs out.
+        if (!(p.hold_lists && k == 0))
+            mbar_arrive(bar0 + 8 * (B_LFULL0 + b));
         if (p.prefetch_rows) {
             SegIter la = it;
             Seg sn;
@@ -761,7 +764,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 // (m in log2 units, O unnormalised):
 //   M = max(sink*log2e, max_s m_s);  w_s = 2^(m_s - M)
 //   o = sum_s w_s O_s / (sum_s w_s l_s + 2^(sink*log2e - M))
-constexpr int MAX_PIECES = SA_MAX_K / 128 + 2;
+constexpr int MAX_PIECES = SA_MAX_K / 128;
 constexpr int COMBINE_HEADS = 4;   // heads per block: grid (B*T, 64 / COMBINE_HEADS)
 
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p)
@@ -771,16 +774,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ At
     __shared__ int slots[MAX_PIECES];
     const int64_t q = blockIdx.x;
     const int h0 = blockIdx.y * COMBINE_HEADS;
-    const int64_t e0 = q * p.K, e1 = e0 + p.K;
-    const int c0 = (int)(e0 / p.per_cta), c1 = (int)((e1 - 1) / p.per_cta);
-    if (c0 == c1)
-        return;   // one CTA held the whole list and wrote the output itself
-    const int np = c1 - c0 + 1;
+    const int np = p.pieces;   // the query's pieces sit in slots q*pieces .. q*pieces + pieces - 1
     const int t = threadIdx.x;
-    if (t < np) {
-        const int c = c0 + t;
-        slots[t] = ((int64_t)c * p.per_cta >= e0) ? 2 * c : 2 * c + 1;
-    }
+    if (t < np)
+        slots[t] = (int)(q * p.pieces + t);
     __syncthreads();
     if (t < COMBINE_HEADS) {
         const int h = h0 + t;
@@ -847,20 +844,27 @@ Schedule attn_schedule(int64_t BT, int K, int num_sms)
     Schedule s{};
     if (num_sms < 1)
         num_sms = 1;
-    if (BT >= num_sms || K == 0) {
+    // Fewer queries than SMs: cut each list into equal pieces (at least one
+    // 128-row chunk each) so that about every SM holds one piece.
+    int pieces = 1;
+    if (BT > 0 && BT < num_sms && K > 0) {
+        const int64_t by_sms = num_sms / BT;
+        const int64_t by_len = (K + 127) / 128;
+        pieces = (int)(by_sms < by_len ? by_sms : by_len);
+        if (pieces < 1)
+            pieces = 1;
+    }
+    if (pieces == 1) {
         s.split = 0;
         s.grid = (int)(BT < num_sms ? BT : num_sms);
         s.per_cta = 0;
+        s.pieces = 1;
         return s;
     }
-    const int64_t total = BT * K;
-    int64_t e = (total + num_sms - 1) / num_sms;
-    if (e < 128)
-        e = 128;
-    e = (e + 31) / 32 * 32;
     s.split = 1;
-    s.per_cta = e;
-    s.grid = (int)((total + e - 1) / e);
+    s.pieces = pieces;
+    s.per_cta = ((K + pieces - 1) / pieces + 31) / 32 * 32;
+    s.grid = (int)(BT * pieces);
     return s;
 }
 
@@ -869,7 +873,7 @@ size_t attn_workspace_bytes(int64_t BT, int K, int num_sms)
     const Schedule s = attn_schedule(BT, K, num_sms);
     size_t bytes = WS_HEADER;
     if (s.split)
-        bytes += (size_t)2 * s.grid * PART_STRIDE * sizeof(float);
+        bytes += (size_t)s.grid * PART_STRIDE * sizeof(float);
     return (bytes + 255) / 256 * 256;
 }
 
@@ -881,6 +885,7 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
         return ea;
     p.split = s.split;
     p.per_cta = s.per_cta;
+    p.pieces = s.pieces;
     if (s.grid == 0)
         return cudaSuccess;
     attn::attn_kernel<<<s.grid, attn::THREADS, attn::SMEM_BYTES, st>>>(p);

@@ -33,10 +33,12 @@ struct AttnParams {
     int64_t BT;                // B * T
     int T, N, K;
     int out_f32;
-    int split;                 // 0: whole queries, CTA i takes i, i+grid, ...; 1: entry ranges
-    int64_t per_cta;           // split: raw list entries per CTA
+    int split;                 // 0: whole queries, CTA i takes i, i+grid, ...; 1: list pieces
+    int64_t per_cta;           // split: list entries per piece (the last piece may be shorter)
+    int pieces;                // split: pieces per query; CTA c takes piece c % pieces of query c / pieces
     int rope_dim;              // 0 = no rotary epilogue
     int prefetch_rows;         // 1: warm L2 with the next segment's rows (kv larger than L2)
+    int hold_lists;            // failure-detection test hook: never publish the first index list
     uint64_t timeout_ns;       // bound on every device-side wait
 };
 
@@ -44,6 +46,7 @@ struct Schedule {
     int grid;
     int split;
     int64_t per_cta;
+    int pieces;
 };
 
 // Decide the grid and the split of the index lists for this shape and device.
