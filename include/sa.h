@@ -62,8 +62,9 @@ typedef enum { SA_BF16 = 0, SA_F32 = 1 } sa_dtype;
 
 /*
  * Bytes of workspace `sa_sparse_attn` needs for this shape on the current
- * device (the split-query partial results depend on its SM count).  Always a
- * multiple of 256 and at least 256 (the error word).
+ * device.  Always a multiple of 256 and at least 256 (the error word); the
+ * size may depend on the shape and on the device's SM count, so query it
+ * rather than assuming the minimum.
  */
 size_t sa_sparse_attn_workspace_size(int B, int T, int H, int D, int K);
 
@@ -130,11 +131,11 @@ sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim,
  * real-time loop that must not enter the driver's allocator).  The pages have
  * no counterpart: this is a convenience of this library.
  *
- * The scratch is a 40 MiB array in the library's device image: every process
+ * The scratch is a 64 KiB array in the library's device image: every process
  * that loads the library holds it on every GPU it uses, until exit.  Shapes
- * whose scratch (sa_sparse_attn_workspace_size) exceeds 40 MiB return
- * SA_ERR_WORKSPACE before anything is enqueued; on GB300 every shape
- * sa_sparse_attn accepts fits.  Nothing is allocated: no cudaMalloc, no
+ * whose scratch (sa_sparse_attn_workspace_size) exceeds 64 KiB return
+ * SA_ERR_WORKSPACE before anything is enqueued; every shape sa_sparse_attn
+ * accepts needs 256 bytes.  Nothing is allocated: no cudaMalloc, no
  * cudaFree, no allocating library routine.
  *
  * The first call on a device looks up the array's device address (with that

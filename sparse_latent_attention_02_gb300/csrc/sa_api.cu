@@ -58,7 +58,6 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const f
     p.sink = sink;
     p.out = out;
     p.err = static_cast<uint32_t *>(ws);
-    p.part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + WS_HEADER);
     p.scale_log2 = scale * 1.4426950408889634f;
     p.BT = (int64_t)B * T;
     p.T = T;

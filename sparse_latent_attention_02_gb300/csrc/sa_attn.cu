@@ -47,7 +47,9 @@ constexpr int NUM_GATHER_WARPS = 16;
 constexpr int WARP_GATHER0 = 4;                 // warps 4 .. 19
 constexpr int WARP_CONTROL = 20, WARP_MMA = 21; // warps 22, 23 only lend registers
 constexpr int THREADS = 24 * 32;
-constexpr int ROWS_PER_GATHER_WARP = CH / NUM_GATHER_WARPS;   // 8
+constexpr int MAX_CLUSTER = 8;                                // list pieces of one query
+constexpr int GATHER_GROUP_WARPS = NUM_GATHER_WARPS / 2;          // each group owns two tiles
+constexpr int ROWS_PER_GATHER_WARP = CH / GATHER_GROUP_WARPS;     // 16
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
 
@@ -67,7 +69,10 @@ constexpr uint32_t OFF_AUX = OFF_M + 64 * 4;           // float [64] factors / 1
 constexpr uint32_t OFF_SEGN = OFF_AUX + 64 * 4;        // int [2] list lengths
 constexpr uint32_t OFF_BAR = OFF_SEGN + 16;            // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;        // [0] TMEM base, [1] abort flag
-constexpr uint32_t SMEM_USED = OFF_MISC + 64;
+constexpr uint32_t OFF_RAW = OFF_MISC + 64;           // int32 [SA_MAX_K] list as read from idx
+constexpr uint32_t OFF_XSTAT = OFF_RAW + 4 * SA_MAX_K;   // float [pieces][2][64 / pieces] peers' (m, l)
+constexpr uint32_t OFF_XSEND = OFF_XSTAT + 2 * 64 * 4;   // float [2][64 / pieces] (m, l) being sent
+constexpr uint32_t SMEM_USED = OFF_XSEND + 2 * 64 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -83,6 +88,8 @@ enum : uint32_t {
     B_LFULL0,
     B_LEMPTY0 = B_LFULL0 + 2,
     B_DONE = B_LEMPTY0 + 2,
+    B_XRDY,      // split schedule: every peer's chunk buffer is free to receive
+    B_XFULL,     // split schedule: every peer's partial for this CTA's heads has arrived (bytes)
     NUM_BARS
 };
 constexpr uint32_t LEMPTY_ARRIVALS = NUM_GATHER_WARPS + 1 + 4;   // gather warps, MMA, softmax warps
@@ -98,7 +105,6 @@ struct Seg {
     int64_t q;
     int j0, j1;
     bool full;
-    int slot;
 };
 
 struct SegIter {
@@ -115,7 +121,7 @@ __device__ __forceinline__ void seg_begin(const AttnParams &p, SegIter &it)
 
 // Whole mode: CTA i takes queries i, i + grid, ...  Split mode: CTA c takes
 // piece c % pieces (entries [i*per_cta, min((i+1)*per_cta, K))) of query
-// c / pieces and leaves its partial result in slot c.
+// c / pieces; the pieces of a query are the CTAs of one cluster, rank = piece.
 __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &s)
 {
     if (!p.split) {
@@ -125,7 +131,6 @@ __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &
         s.j0 = 0;
         s.j1 = p.K;
         s.full = true;
-        s.slot = -1;
         it.q += gridDim.x;
         return true;
     }
@@ -134,55 +139,61 @@ __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &
     it.done = true;
     const int piece = (int)(blockIdx.x % (unsigned)p.pieces);
     s.q = blockIdx.x / p.pieces;
-    s.j0 = (int)(piece * p.per_cta);
+    // an empty piece still takes part in its cluster's merge (with no rows)
+    s.j0 = (int)min((int64_t)p.K, piece * p.per_cta);
     s.j1 = (int)min((int64_t)p.K, (piece + 1) * p.per_cta);
     s.full = false;
-    s.slot = (int)blockIdx.x;
-    return s.q < p.BT && s.j0 < s.j1;
+    return s.q < p.BT;
 }
 
-// Keep the entries of idx[q, j0:j1] that are inside [0, N), in list order, in
-// cidx; `bad` is set if an entry other than -1 falls outside [0, N).
-__device__ __forceinline__ int compact_list(const int32_t *il, int j0, int j1, int N, int32_t *cidx,
-                                            int lane, bool &bad)
+// Start copying idx[q, j0:j1] into the staging buffer (whole warp, one
+// 4-byte cp.async per entry, all in flight at once: one memory round trip).
+__device__ __forceinline__ void stage_list(const AttnParams &p, const Seg &s, uint32_t raw, int lane)
+{
+    const int32_t *il = p.idx + s.q * (int64_t)p.K;
+    for (int j = s.j0 + lane; j < s.j1; j += 32)
+        cp_async4(raw + 4u * (uint32_t)(j - s.j0), il + j);
+    cp_async_commit();
+}
+
+// Keep the staged entries that are inside [0, N), in list order, in cidx;
+// `bad` is set if an entry other than -1 falls outside [0, N).
+__device__ __forceinline__ int compact_staged(const int32_t *raw, int len, int N, int32_t *cidx, int lane,
+                                              bool &bad)
 {
     int n = 0;
-    for (int j = j0; j < j1; j += 256) {
-        int v[8];
+    const uint32_t below = (1u << lane) - 1u;
+    for (int j = 0; j < len; j += 128) {
+        int v[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
             const int jj = j + 32 * u + lane;
-            v[u] = jj < j1 ? __ldg(il + jj) : -1;
+            v[u] = jj < len ? raw[jj] : -1;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 4; ++u) {
             const bool valid = v[u] >= 0 && v[u] < N;
             bad |= v[u] < -1 || v[u] >= N;
             const uint32_t m = __ballot_sync(0xffffffffu, valid);
             if (valid)
-                cidx[n + __popc(m & ((1u << lane) - 1u))] = v[u];
+                cidx[n + __popc(m & below)] = v[u];
             n += __popc(m);
         }
     }
     return n;
 }
 
-// Warm L2 with the latent rows a segment will gather (whole warp).
-__device__ __forceinline__ void prefetch_segment_rows(const AttnParams &p, const Seg &s, int lane)
+// Warm L2 with latent rows (whole warp, one line prefetch per 128 bytes):
+// rows list[j0 .. j1) of batch element bidx, skipping entries outside [0, N).
+__device__ __forceinline__ void prefetch_rows(const AttnParams &p, int64_t bidx, const int32_t *list, int j0,
+                                              int j1, int lane)
 {
-    const int32_t *il = p.idx + s.q * (int64_t)p.K;
-    const uint16_t *kvb = p.kv + (size_t)(s.q / p.T) * (size_t)p.N * D;
-    for (int j = s.j0; j < s.j1; j += 256) {
-        int v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int jj = j + 32 * u + lane;
-            v[u] = jj < s.j1 ? __ldg(il + jj) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (v[u] >= 0 && v[u] < p.N)
-                prefetch_l2(kvb + (size_t)v[u] * D, D * 2);
+    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv + (size_t)bidx * (size_t)p.N * D);
+    // lane = 8 * (row within a group of 4) + line
+    for (int j = j0 + (lane >> 3); j < j1; j += 4) {
+        const int v = list[j];
+        if (v >= 0 && v < p.N)
+            prefetch_l2_line(kvb + (size_t)v * (D * 2) + (lane & 7) * 128);
     }
 }
 
@@ -236,22 +247,49 @@ __device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane, int &hea
 
 // ------------------------------------------------------------------ roles
 
-// Warp 20: compacts every segment's index list (double-buffered), publishes
-// its length, and loads the segment's Q by TMA.
+// Wait until the previous segment's QK products are done with Q, then load
+// this segment's Q (64 heads x 512 features) by TMA (whole warp, lane 0 issues).
+__device__ __forceinline__ bool load_q(const AttnParams &p, uint32_t sbase, const Seg &s, uint32_t &ph_qempty,
+                                       uint32_t &q_loads, volatile int *abort_flag, int lane)
+{
+    const uint32_t bar0 = sbase + OFF_BAR;
+    const bool ok = warp_wait(bar0 + 8 * B_QEMPTY, ph_qempty ^ 1u, abort_flag, p.timeout_ns, lane);
+    ph_qempty ^= 1u;
+    if (!ok)
+        return false;
+    if (lane == 0) {
+        const uint32_t bq = bar0 + 8 * B_QFULL;
+        mbar_arrive_expect_tx(bq, Q_BYTES);
+        for (int kb = 0; kb < 8; ++kb)
+            tma_load_2d(sbase + OFF_Q + kb * QBLK_BYTES, &p.tm_q, kb * 64, (int32_t)(s.q * H), bq);
+    }
+    ++q_loads;
+    return true;
+}
+
+// Warp 20: loads every segment's Q by TMA and its index list into the
+// staging buffer, compacts the list into a double-buffered shared list and
+// publishes its length.  When kv is larger than L2 it then warms L2 with the
+// next segment's rows while the current segment is processed.
 __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int lane,
                              volatile int *abort_flag)
 {
     int *segn = reinterpret_cast<int *>(smem + OFF_SEGN);
+    const int32_t *raw = reinterpret_cast<const int32_t *>(smem + OFF_RAW);
+    const uint32_t raw_u32 = sbase + OFF_RAW;
     const uint32_t bar0 = sbase + OFF_BAR;
     uint32_t ph_qempty = 0, ph_lempty[2] = {0, 0};
     uint32_t q_loads = 0;
     bool ok = true;
     SegIter it;
     seg_begin(p, it);
-    Seg s;
+    Seg s, sn;
     bool have = seg_next(p, it, s);
-    if (have && p.prefetch_rows)
-        prefetch_segment_rows(p, s, lane);
+    if (have) {
+        stage_list(p, s, raw_u32, lane);
+        // the first segment's Q is requested before its list is read
+        ok = load_q(p, sbase, s, ph_qempty, q_loads, abort_flag, lane);
+    }
     for (int k = 0; ok && have; ++k) {
         const int b = k & 1;
         // every consumer of this list buffer is done with the segment before
@@ -259,9 +297,11 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         ph_lempty[b] ^= 1u;
         if (!ok)
             break;
+        cp_async_wait_all();
+        __syncwarp();
         int32_t *cidx = reinterpret_cast<int32_t *>(smem + OFF_IDX) + b * SA_MAX_K;
         bool bad = false;
-        const int n = compact_list(p.idx + s.q * (int64_t)p.K, s.j0, s.j1, p.N, cidx, lane, bad);
+        const int n = compact_staged(raw, s.j1 - s.j0, p.N, cidx, lane, bad);
         if (__any_sync(0xffffffffu, bad) && lane == 0)
             atomicOr(p.err, ERRBIT_INDEX);
         if (lane == 0)
@@ -272,47 +312,48 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         // runs out.
         if (!(p.hold_lists && k == 0))
             mbar_arrive(bar0 + 8 * (B_LFULL0 + b));
-        if (p.prefetch_rows) {
-            SegIter la = it;
-            Seg sn;
-            if (seg_next(p, la, sn))
-                prefetch_segment_rows(p, sn, lane);
-        }
-        if (n > 0) {
-            // Q of this query, once the previous segment's QK products are done with it
-            ok = warp_wait(bar0 + 8 * B_QEMPTY, ph_qempty ^ 1u, abort_flag, p.timeout_ns, lane);
-            ph_qempty ^= 1u;
+        // Q of a later segment, once the previous segment's QK products are done with it
+        if (k > 0) {
+            ok = load_q(p, sbase, s, ph_qempty, q_loads, abort_flag, lane);
             if (!ok)
                 break;
-            if (lane == 0) {
-                const uint32_t bq = bar0 + 8 * B_QFULL;
-                mbar_arrive_expect_tx(bq, Q_BYTES);
-                for (int kb = 0; kb < 8; ++kb)
-                    tma_load_2d(sbase + OFF_Q + kb * QBLK_BYTES, &p.tm_q, kb * 64, (int32_t)(s.q * H), bq);
-            }
-            ++q_loads;
         }
-        have = seg_next(p, it, s);
+        have = seg_next(p, it, sn);
+        if (have) {
+            stage_list(p, sn, raw_u32, lane);
+            if (p.prefetch_rows) {
+                cp_async_wait_all();
+                __syncwarp();
+                prefetch_rows(p, sn.q / p.T, raw, 0, sn.j1 - sn.j0, lane);
+            }
+            s = sn;
+        }
     }
+    cp_async_wait_all();
     // a Q load still in flight must land before the CTA can exit
     if (lane == 0 && q_loads > 0)
         drain_wait(bar0 + 8 * B_QFULL, (q_loads - 1u) & 1u, p.timeout_ns);
     __syncwarp();
 }
 
-// Warps 4-19: gather the compacted rows, chunk by chunk, tile by tile (two
-// 64-feature slices of the 128 rows per tile).  Warp gi copies rows
-// 8gi .. 8gi+7; rows past the end of the list are zero-filled.
+// Warps 4-19: gather the compacted rows, chunk by chunk, in two groups of
+// eight warps: group g fills tiles g and g + 2 (a tile is two 64-feature
+// slices of the 128 rows), so all four tiles of a chunk can be in flight at
+// once and each tile is refilled as soon as the PV product frees it.  Warp w
+// of a group copies rows 16w .. 16w+15; rows past the end of the list are
+// zero-filled.
 __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int gi, int lane,
                             volatile int *abort_flag)
 {
     const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
     const uint32_t bar0 = sbase + OFF_BAR;
-    uint32_t ph_lfull[2] = {0, 0}, ph_kvfree[4] = {0, 0, 0, 0};
+    const int grp = gi / GATHER_GROUP_WARPS, wg = gi % GATHER_GROUP_WARPS;
+    uint32_t ph_lfull[2] = {0, 0}, ph_kvfree[2] = {0, 0};
     bool ok = true;
     SegIter it;
     seg_begin(p, it);
     Seg s;
+    const int pc = lane & 15;   // piece: slice (2d + pc / 8), 16-byte chunk pc % 8
     for (int k = 0; ok && seg_next(p, it, s); ++k) {
         const int b = k & 1;
         ok = warp_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns, lane);
@@ -325,43 +366,54 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
         const uint16_t *kvb = p.kv + (size_t)(s.q / p.T) * (size_t)p.N * D;
         for (int c = 0; c < nc && ok; ++c) {
             const int rows = min(CH, n - c * CH);
-            // this lane's four (row, 16-byte piece) jobs; the rows are the same for every tile
-            int r[4], row[4];
+            // this lane's eight (row, 16-byte piece) jobs; the rows are the same for both tiles
+            int r[8], row[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                r[i] = ROWS_PER_GATHER_WARP * gi + ((i * 32 + lane) >> 4);
+            for (int i = 0; i < 8; ++i) {
+                r[i] = ROWS_PER_GATHER_WARP * wg + 2 * i + (lane >> 4);
                 row[i] = r[i] < rows ? cidx[c * CH + r[i]] : -1;
             }
-            const int pc = lane & 15;   // piece: slice (2d + pc / 8), 16-byte chunk pc % 8
-            for (int d = 0; d < 4; ++d) {
-                ok = warp_wait(bar0 + 8 * (B_KVFREE0 + d), ph_kvfree[d] ^ 1u, abort_flag, p.timeout_ns,
-                               lane);
-                ph_kvfree[d] ^= 1u;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int d = grp + 2 * e;
+                ok = warp_wait(bar0 + 8 * (B_KVFREE0 + d), ph_kvfree[e] ^ 1u, abort_flag, p.timeout_ns, lane);
+                ph_kvfree[e] ^= 1u;
                 if (!ok)
                     break;
                 const int sl = 2 * d + (pc >> 3), ch = pc & 7;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r[i] * 128 + ((ch ^ (r[i] & 7)) << 4);
                     const uint16_t *src = kvb + (size_t)(row[i] < 0 ? 0 : row[i]) * D + sl * 64 + ch * 8;
                     cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
                 }
                 cp_async_commit();
-                if (d > 0) {
-                    cp_async_wait<1>();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar0 + 8 * (B_KVFULL0 + d - 1));
-                }
             }
             if (!ok)
                 break;
+            cp_async_wait<1>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar0 + 8 * (B_KVFULL0 + grp));
             cp_async_wait<0>();
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(bar0 + 8 * (B_KVFULL0 + 3));
+                mbar_arrive(bar0 + 8 * (B_KVFULL0 + grp + 2));
+            // kv larger than L2: this chunk has landed; start bringing this warp's
+            // part of the next chunk (its rows, its two tiles' 128-byte lines) into
+            // L2 while the chunk is used, so that the refill after the PV product
+            // does not wait for HBM
+            if (p.prefetch_rows && c + 1 < nc) {
+                const int j = (c + 1) * CH + ROWS_PER_GATHER_WARP * wg + (lane >> 1);
+                if (j < n) {
+                    const uint8_t *rp = reinterpret_cast<const uint8_t *>(kvb + (size_t)cidx[j] * D) +
+                                        (grp + 2 * (lane & 1)) * 256;
+                    prefetch_l2_line(rp);
+                    prefetch_l2_line(rp + 128);
+                }
+            }
         }
         if (!ok)
             break;
@@ -403,12 +455,15 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uin
         const int n = segn[b];
         mbar_arrive(bar0 + 8 * (B_LEMPTY0 + b));
         const int nc = (n + CH - 1) / CH;
-        if (nc == 0)
-            continue;
+        // Q is loaded for every segment
         ok = bounded_wait(bar0 + 8 * B_QFULL, ph_qfull, abort_flag, p.timeout_ns);
         ph_qfull ^= 1u;
         if (!ok)
             break;
+        if (nc == 0) {
+            mbar_arrive(bar0 + 8 * B_QEMPTY);
+            continue;
+        }
         for (int c = 0; c < nc && ok; ++c) {
             // S^T = K_chunk . Q^T over 32 steps of 16 features, tile by tile as they land
 #pragma unroll
@@ -462,6 +517,192 @@ __device__ void mma_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uin
     // every MMA issued must complete before TMEM is released
     mma_commit(bar0 + 8 * B_DONE);
     drain_wait(bar0 + 8 * B_DONE, 0, p.timeout_ns);
+}
+
+// Warp-uniform bounded wait for arrivals from other CTAs of the cluster.
+__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                  uint64_t limit_ns, int lane)
+{
+    int ok = 0;
+    if (lane == 0)
+        ok = bounded_wait_cluster(bar, parity, abort_flag, limit_ns) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Split schedule: the P pieces of one query's list run as one cluster, and
+// CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  Every
+// CTA sends each peer its unnormalised O^T columns and its (m, l) for that
+// peer's heads into the peer's chunk buffer: it stages them in its own slot
+// of its own chunk buffer (the slot no peer writes) and moves them with one
+// bulk shared-to-shared copy per peer, which completes on the peer's XFULL
+// barrier.  A CTA offers its buffer (arrives on each peer's XRDY barrier)
+// once its own last PV product is done.  The receiver merges the pieces:
+//   M = max_r m_r (each m_r starts at the sink),  w_r = 2^(m_r - M),
+//   o = sum_r w_r O_r / (sum_r w_r l_r + 2^(sink*log2e - M))
+// then applies the inverse RoPE when asked and writes its heads.  Softmax
+// warpgroup only (thread t = TMEM lane t); false when a wait ran out.
+template <int P>
+__device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl, const Seg &s,
+                              int nc, int t, volatile int *abort_flag, int lane)
+{
+    constexpr int HP = H / P;
+    constexpr uint32_t SLOT_BYTES = HP * D * 4;      // one piece's O for HP heads, [HP][512] fp32
+    constexpr uint32_t STAT_BYTES = 2 * HP * 4;      // its (m, l) for HP heads
+    const uint32_t me = cluster_ctarank();
+    const uint32_t bar0 = sbase + OFF_BAR;
+    const float *m_s = reinterpret_cast<const float *>(smem + OFF_M);
+    const float *lt = reinterpret_cast<const float *>(smem + OFF_AUX);   // this piece's row sums
+    const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);
+    float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights, then [HP] 1/den
+    const float *recv = reinterpret_cast<const float *>(smem + OFF_KV);   // [P][HP][512] fp32
+    float *stage = reinterpret_cast<float *>(smem + OFF_KV + me * SLOT_BYTES);
+    float *xsend = reinterpret_cast<float *>(smem + OFF_XSEND);
+
+    if (t == 0)
+        mbar_arrive_expect_tx(bar0 + 8 * B_XFULL, (P - 1) * (SLOT_BYTES + STAT_BYTES));
+    if (t < P && t != (int)me)
+        mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
+    bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
+    if (bar_red_or(1, 128, !ok || *abort_flag))
+        return false;
+
+    // send: peer g gets columns g*HP .. g*HP + HP-1 of every 128-feature tile
+    bool first = true;
+    for (int g = 0; g < P; ++g) {
+        if (g == (int)me)
+            continue;
+        if (!first) {
+            // the previous copy has finished reading the staging slot
+            if (t == 0)
+                bulk_wait_read_all();
+            bar_sync(1, 128);
+        }
+        first = false;
+        if (t < HP) {
+            xsend[t] = m_s[g * HP + t];
+            xsend[HP + t] = lt[g * HP + t];
+        }
+#pragma unroll 1
+        for (int d = 0; d < 4; ++d) {
+            uint32_t v[HP];
+            if (nc > 0) {
+#pragma unroll
+                for (int j = 0; j < HP / 8; ++j)
+                    tmem_ld8(tl + TM_O + 64 * d + g * HP + 8 * j, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * j]));
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < HP; ++i)
+                    v[i] = 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < HP; ++i)
+                stage[i * D + 128 * d + t] = __uint_as_float(v[i]);
+        }
+        fence_proxy_async_smem();
+        bar_sync(1, 128);
+        if (t == 0) {
+            const uint32_t rbar = mapa_shared(bar0 + 8 * B_XFULL, (uint32_t)g);
+            bulk_copy_to_peer(mapa_shared(sbase + OFF_KV + me * SLOT_BYTES, (uint32_t)g),
+                              sbase + OFF_KV + me * SLOT_BYTES, SLOT_BYTES, rbar);
+            bulk_copy_to_peer(mapa_shared(sbase + OFF_XSTAT + me * STAT_BYTES, (uint32_t)g),
+                              sbase + OFF_XSEND, STAT_BYTES, rbar);
+            bulk_commit();
+        }
+    }
+    if (t == 0)
+        bulk_wait_read_all();
+
+    ok = warp_wait_cluster(bar0 + 8 * B_XFULL, 0, abort_flag, p.timeout_ns, lane);
+    if (bar_red_or(1, 128, !ok || *abort_flag))
+        return false;
+
+    if (t < HP) {
+        const int h = (int)me * HP + t;
+        const float sl = __ldg(p.sink + h) * LOG2E;
+        float M = m_s[h];
+#pragma unroll
+        for (int r = 0; r < P; ++r)
+            if (r != (int)me)
+                M = fmaxf(M, xst[r * 2 * HP + t]);
+        float den = 0.f;
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            const float mr = r == (int)me ? m_s[h] : xst[r * 2 * HP + t];
+            const float lr = r == (int)me ? lt[h] : xst[r * 2 * HP + HP + t];
+            const float w = M == -INFINITY ? 0.f : ex2(mr - M);
+            wts[r * HP + t] = w;
+            den += w * lr;
+        }
+        den += M == -INFINITY ? 0.f : ex2(sl - M);
+        wts[P * HP + t] = den > 0.f ? 1.f / den : 0.f;
+    }
+    bar_sync(1, 128);
+
+    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
+#pragma unroll 1
+    for (int d = 0; d < 4; ++d) {
+        const int f = 128 * d + t;
+        uint32_t v[HP];
+        if (nc > 0) {
+#pragma unroll
+            for (int j = 0; j < HP / 8; ++j)
+                tmem_ld8(tl + TM_O + 64 * d + me * HP + 8 * j, *reinterpret_cast<uint32_t(*)[8]>(&v[8 * j]));
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < HP; ++i)
+                v[i] = 0u;
+        }
+        float o[HP];
+#pragma unroll
+        for (int i = 0; i < HP; ++i)
+            o[i] = wts[me * HP + i] * __uint_as_float(v[i]);
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            if (r == (int)me)
+                continue;
+#pragma unroll
+            for (int i = 0; i < HP; ++i)
+                o[i] += wts[r * HP + i] * recv[(r * HP + i) * 512 + f];
+        }
+#pragma unroll
+        for (int i = 0; i < HP; ++i)
+            o[i] *= wts[P * HP + i];
+        if (p.rope_dim > 0 && f >= D - p.rope_dim) {   // warp-uniform
+            const int pi = (f - (D - p.rope_dim)) >> 1;
+            const float *cs = p.rope + ((size_t)(s.q % p.T) * (p.rope_dim >> 1) + pi) * 2;
+            const float cth = __ldg(cs), sth = __ldg(cs + 1);
+            const bool odd = f & 1;
+#pragma unroll
+            for (int i = 0; i < HP; ++i) {
+                const float other = __shfl_xor_sync(0xffffffffu, o[i], 1);
+                o[i] = odd ? (o[i] * cth - other * sth) : (o[i] * cth + other * sth);
+            }
+        }
+        if (p.out_f32) {
+            float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + (size_t)(me * HP) * D + f;
+#pragma unroll
+            for (int i = 0; i < HP; ++i)
+                po[i * D] = o[i];
+        } else {
+            // stage [HP heads][128 features] bf16, then write 256-byte head rows with 16-byte stores
+#pragma unroll
+            for (int i = 0; i < HP; ++i)
+                stg[i * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(o[i]));
+            bar_sync(1, 128);
+            uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + (size_t)(me * HP) * D + 128 * d) * 2;
+#pragma unroll
+            for (int j = 0; j < HP / 8; ++j) {
+                const int c = t + 128 * j;   // 16-byte piece c: head c / 16, part c % 16
+                const int h = c >> 4, part = c & 15;
+                const uint4 val = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
+                *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = val;
+            }
+            bar_sync(1, 128);
+        }
+    }
+    return true;
 }
 
 __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tmem,
@@ -616,32 +857,46 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 const float den = lt + ex2(__ldg(p.sink + t) * LOG2E - m_s[t]);
                 aux[t] = lt > 0.f ? 1.f / den : 0.f;
             } else {
-                float *pm = p.part + (size_t)s.slot * PART_STRIDE + PART_O;
-                pm[t] = m_s[t];
-                pm[64 + t] = lt;
-                aux[t] = 1.f;
+                aux[t] = lt;
             }
         }
         bar_sync(1, 128);
 
-        // epilogue: thread t owns feature 128*d + t of every head; TMEM is read
-        // in halves of 32 heads
-        const bool rope_here = s.full && p.rope_dim > 0;
+        if (!s.full) {
+            bool mok = false;
+            switch (p.pieces) {
+            case 2: mok = cluster_merge<2>(p, smem, sbase, tl, s, nc, t, abort_flag, lane); break;
+            case 4: mok = cluster_merge<4>(p, smem, sbase, tl, s, nc, t, abort_flag, lane); break;
+            case 8: mok = cluster_merge<8>(p, smem, sbase, tl, s, nc, t, abort_flag, lane); break;
+            default: break;
+            }
+            if (!mok)
+                break;
+            if (nc > 0) {
+                tc_fence_before();
+                mbar_arrive(bar0 + 8 * B_OFREE);
+            }
+            continue;
+        }
+
+        // epilogue: thread t owns feature 128*d + t of every head; both 32-head
+        // halves of a tile are read from TMEM before one wait
+        const bool rope_here = p.rope_dim > 0;
         uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
 #pragma unroll 1
-        for (int e = 0; e < 8; ++e) {
-            const int d = e >> 1, hh = e & 1;
+        for (int d = 0; d < 4; ++d) {
             const int dim = 128 * d + t;
-            uint32_t u[32];
+            uint32_t u[64];
             if (nc > 0) {
-                tmem_ld32(tl + TM_O + 32 * e, u);
+                tmem_ld32(tl + TM_O + 64 * d, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+                tmem_ld32(tl + TM_O + 64 * d + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    u[i] = __float_as_uint(__uint_as_float(u[i]) * aux[32 * hh + i]);
+                for (int i = 0; i < 64; ++i)
+                    u[i] = __float_as_uint(__uint_as_float(u[i]) * aux[i]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
+                for (int i = 0; i < 64; ++i)
                     u[i] = 0u;
             }
             if (rope_here && dim >= D - p.rope_dim) {   // warp-uniform
@@ -650,41 +905,34 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 const float cth = __ldg(cs), sth = __ldg(cs + 1);
                 const bool odd = dim & 1;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 64; ++i) {
                     const float o = __uint_as_float(u[i]);
                     const float other = __shfl_xor_sync(0xffffffffu, o, 1);
                     u[i] = __float_as_uint(odd ? (o * cth - other * sth) : (o * cth + other * sth));
                 }
             }
-            if (!s.full) {
-                float *po = p.part + (size_t)s.slot * PART_STRIDE + (size_t)(32 * hh) * 512 + dim;
+            if (p.out_f32) {
+                float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + dim;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    po[i * 512] = __uint_as_float(u[i]);
-            } else if (p.out_f32) {
-                float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + (size_t)(32 * hh) * 512 + dim;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
+                for (int i = 0; i < 64; ++i)
                     po[i * 512] = __uint_as_float(u[i]);
             } else {
                 // stage the tile as [64 heads][128 features] bf16 in the P buffer
-                // (free once the last PV is done); after both halves, write whole
-                // 256-byte head rows with 16-byte stores
+                // (free once the last PV is done), then write whole 256-byte head
+                // rows with 16-byte stores
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    stg[(32 * hh + i) * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[i])));
-                if (hh == 1) {
-                    bar_sync(1, 128);
-                    uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
+                for (int i = 0; i < 64; ++i)
+                    stg[i * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[i])));
+                bar_sync(1, 128);
+                uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int c = t + 128 * i;   // 16-byte piece c: head c / 16, part c % 16
-                        const int h = c >> 4, part = c & 15;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
-                        *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
-                    }
-                    bar_sync(1, 128);
+                for (int i = 0; i < 8; ++i) {
+                    const int c = t + 128 * i;   // 16-byte piece c: head c / 16, part c % 16
+                    const int h = c >> 4, part = c & 15;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
+                    *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
                 }
+                bar_sync(1, 128);
             }
         }
         if (nc > 0) {
@@ -709,7 +957,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         mbar_init(bar0 + 8 * B_QFULL, 1);
         mbar_init(bar0 + 8 * B_QEMPTY, 1);
         for (int d = 0; d < 4; ++d) {
-            mbar_init(bar0 + 8 * (B_KVFULL0 + d), NUM_GATHER_WARPS);
+            mbar_init(bar0 + 8 * (B_KVFULL0 + d), GATHER_GROUP_WARPS);
             mbar_init(bar0 + 8 * (B_KVFREE0 + d), 1);
         }
         mbar_init(bar0 + 8 * B_SFULL, 1);
@@ -721,6 +969,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             mbar_init(bar0 + 8 * (B_LEMPTY0 + b), LEMPTY_ARRIVALS);
         }
         mbar_init(bar0 + 8 * B_DONE, 1);
+        mbar_init(bar0 + 8 * B_XRDY, p.split ? (uint32_t)(p.pieces - 1) : 1u);
+        mbar_init(bar0 + 8 * B_XFULL, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);
@@ -733,6 +983,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the peers' barriers are initialised before any CTA of the cluster arrives on them
+    if (p.split) {
+        __syncwarp();
+        cluster_sync();
+    }
 
     if (warp < 4) {
         // the softmax warpgroup keeps 64 scores and 64 row sums per thread
@@ -750,88 +1005,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
 
     tc_fence_before();
     __syncthreads();
+    // no CTA leaves while a peer may still write into its shared memory
+    if (p.split) {
+        __syncwarp();
+        cluster_sync();
+    }
     if (threadIdx.x == 0 && *abort_flag)
         atomicOr(p.err, ERRBIT_TIMEOUT);
     if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
-    }
-}
-
-// ------------------------------------------------------------------ split combine
-//
-// For a query whose index list was cut into pieces, merge the pieces' (m, l, O)
-// (m in log2 units, O unnormalised):
-//   M = max(sink*log2e, max_s m_s);  w_s = 2^(m_s - M)
-//   o = sum_s w_s O_s / (sum_s w_s l_s + 2^(sink*log2e - M))
-constexpr int MAX_PIECES = SA_MAX_K / 128;
-constexpr int COMBINE_HEADS = 4;   // heads per block: grid (B*T, 64 / COMBINE_HEADS)
-
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttnParams p)
-{
-    __shared__ float w_s[MAX_PIECES][COMBINE_HEADS];
-    __shared__ float inv_den[COMBINE_HEADS];
-    __shared__ int slots[MAX_PIECES];
-    const int64_t q = blockIdx.x;
-    const int h0 = blockIdx.y * COMBINE_HEADS;
-    const int np = p.pieces;   // the query's pieces sit in slots q*pieces .. q*pieces + pieces - 1
-    const int t = threadIdx.x;
-    if (t < np)
-        slots[t] = (int)(q * p.pieces + t);
-    __syncthreads();
-    if (t < COMBINE_HEADS) {
-        const int h = h0 + t;
-        const float sl = __ldg(p.sink + h) * LOG2E;
-        float M = sl;
-        for (int i = 0; i < np; ++i)
-            M = fmaxf(M, p.part[(size_t)slots[i] * PART_STRIDE + PART_O + h]);
-        float den = 0.f, lsum = 0.f;
-        for (int i = 0; i < np; ++i) {
-            const float *pm = p.part + (size_t)slots[i] * PART_STRIDE + PART_O;
-            const float w = (M == -INFINITY) ? 0.f : ex2(pm[h] - M);
-            w_s[i][t] = w;
-            den += w * pm[64 + h];
-            lsum += pm[64 + h];
-        }
-        den += (M == -INFINITY) ? 0.f : ex2(sl - M);
-        inv_den[t] = (lsum > 0.f && den > 0.f) ? 1.f / den : 0.f;
-    }
-    __syncthreads();
-    // this block's 4 heads x 512 features: 8 consecutive features per thread
-    const int hl = (8 * t) >> 9;
-    const int dim = (8 * t) & 511;
-    const int e = (h0 + hl) * D + dim;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.part + (size_t)slots[i] * PART_STRIDE + e);
-        const float4 a = src[0], b = src[1];
-        const float w = w_s[i][hl];
-        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
-    }
-    float o[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        o[k] = acc[k] * inv_den[hl];
-    if (p.rope_dim > 0 && dim >= D - p.rope_dim) {
-        const float *cs = p.rope + ((size_t)(q % p.T) * (p.rope_dim >> 1) + ((dim - (D - p.rope_dim)) >> 1)) * 2;
-#pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-            const float c = __ldg(cs + k), sn = __ldg(cs + k + 1);
-            const float a = o[k], b = o[k + 1];
-            o[k] = a * c + b * sn;
-            o[k + 1] = -a * sn + b * c;
-        }
-    }
-    if (p.out_f32) {
-        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + q * (H * D) + e);
-        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-    } else {
-        *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) + q * (H * D) + e) =
-            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                       pack_bf16x2(o[6], o[7]));
     }
 }
 
@@ -845,14 +1028,18 @@ Schedule attn_schedule(int64_t BT, int K, int num_sms)
     if (num_sms < 1)
         num_sms = 1;
     // Fewer queries than SMs: cut each list into equal pieces (at least one
-    // 128-row chunk each) so that about every SM holds one piece.
+    // 128-row chunk each), a power of two up to the cluster limit, so that
+    // about every SM holds one piece and the pieces' heads split evenly.
     int pieces = 1;
     if (BT > 0 && BT < num_sms && K > 0) {
-        const int64_t by_sms = num_sms / BT;
+        int64_t lim = num_sms / BT;
         const int64_t by_len = (K + 127) / 128;
-        pieces = (int)(by_sms < by_len ? by_sms : by_len);
-        if (pieces < 1)
-            pieces = 1;
+        if (by_len < lim)
+            lim = by_len;
+        if (lim > attn::MAX_CLUSTER)
+            lim = attn::MAX_CLUSTER;
+        while (pieces * 2 <= lim)
+            pieces *= 2;
     }
     if (pieces == 1) {
         s.split = 0;
@@ -871,10 +1058,8 @@ Schedule attn_schedule(int64_t BT, int K, int num_sms)
 size_t attn_workspace_bytes(int64_t BT, int K, int num_sms)
 {
     const Schedule s = attn_schedule(BT, K, num_sms);
-    size_t bytes = WS_HEADER;
-    if (s.split)
-        bytes += (size_t)s.grid * PART_STRIDE * sizeof(float);
-    return (bytes + 255) / 256 * 256;
+    (void)s;
+    return WS_HEADER;
 }
 
 cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
@@ -888,12 +1073,20 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
     p.pieces = s.pieces;
     if (s.grid == 0)
         return cudaSuccess;
-    attn::attn_kernel<<<s.grid, attn::THREADS, attn::SMEM_BYTES, st>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || !s.split)
-        return e;
-    attn::combine_kernel<<<dim3((unsigned)p.BT, attn::H / attn::COMBINE_HEADS), 256, 0, st>>>(p);
-    return cudaGetLastError();
+    // the pieces of one query form a cluster (they merge through distributed shared memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)s.grid);
+    cfg.blockDim = dim3(attn::THREADS);
+    cfg.dynamicSmemBytes = attn::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)s.pieces;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = s.split ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn::attn_kernel, p);
 }
 
 }  // namespace sa

@@ -13,11 +13,8 @@ namespace sa {
 constexpr uint32_t ERRBIT_INDEX = 1u;
 constexpr uint32_t ERRBIT_TIMEOUT = 2u;
 
-// Workspace layout: [0, 256) header (error word), then the split partials.
+// Workspace layout of the attention call: [0, 256) header (error word).
 constexpr size_t WS_HEADER = 256;
-// One split partial: unnormalised O [64 heads][512] fp32, then m[64], l[64].
-constexpr int PART_O = 64 * 512;
-constexpr int PART_STRIDE = PART_O + 128;
 
 struct AttnParams {
     CUtensorMap tm_q;          // q as 2-D [B*T*H rows, D cols] bf16, box 64x64, 128B swizzle
@@ -26,7 +23,6 @@ struct AttnParams {
     const int32_t *idx;        // int32 [B*T, K]
     const float *sink;         // fp32 [H]
     void *out;                 // [B*T, H, D] bf16 or fp32
-    float *part;               // split partials (workspace)
     uint32_t *err;             // error word (workspace)
     const float *rope;         // fp32 [T, rope_dim/2, 2] or null
     float scale_log2;          // softmax scale * log2(e)
@@ -35,7 +31,8 @@ struct AttnParams {
     int out_f32;
     int split;                 // 0: whole queries, CTA i takes i, i+grid, ...; 1: list pieces
     int64_t per_cta;           // split: list entries per piece (the last piece may be shorter)
-    int pieces;                // split: pieces per query; CTA c takes piece c % pieces of query c / pieces
+    int pieces;                // split: pieces per query (2, 4 or 8), one cluster per query;
+                               // CTA c takes piece c % pieces of query c / pieces
     int rope_dim;              // 0 = no rotary epilogue
     int prefetch_rows;         // 1: warm L2 with the next segment's rows (kv larger than L2)
     int hold_lists;            // failure-detection test hook: never publish the first index list
@@ -53,7 +50,7 @@ struct Schedule {
 Schedule attn_schedule(int64_t BT, int K, int num_sms);
 size_t attn_workspace_bytes(int64_t BT, int K, int num_sms);
 
-// Enqueue the attention kernel (and the split combine when needed).
+// Enqueue the attention kernel (a cluster launch in the split schedule).
 cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st);
 
 struct GemmParams {

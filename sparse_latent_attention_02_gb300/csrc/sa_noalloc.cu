@@ -9,16 +9,16 @@
 // library is loaded.
 //
 // Cost of the convenience: every process that loads this library holds
-// SCRATCH_BYTES (40 MiB) of device memory on every GPU it uses, until exit.
+// SCRATCH_BYTES (64 KiB) of device memory on every GPU it uses, until exit.
 #include <mutex>
 
 #include "sa_internal.h"
 
 namespace {
 
-// 40 MiB holds the error word plus the split partial results of the widest
-// schedule on a GPU with up to 159 SMs (GB300 has 152).
-constexpr size_t SCRATCH_BYTES = 40u << 20;
+// The attention call's workspace is its 256-byte header (the error word):
+// the pieces of a split list merge on chip.  64 KiB leaves room to spare.
+constexpr size_t SCRATCH_BYTES = 64u << 10;
 static __device__ __align__(256) unsigned char g_scratch[SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
@@ -71,8 +71,7 @@ extern "C" sa_status sa_sparse_attn_noalloc(const void *q, const void *kv, const
     if ((int64_t)B * T == 0)
         return SA_OK;
     // The array keeps the previous call's contents: the error word must start
-    // at zero for this call's report.  The split partials need no clearing
-    // (each is written before it is read).
+    // at zero for this call's report.
     if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SA_ERR_CUDA;
     return sa_sparse_attn(q, kv, sink, idx, scale, B, T, H, D, N, K, out, out_dtype, ws,

@@ -47,7 +47,7 @@ def _noalloc(lib, q, kv, sink, idx, out):
 
 
 @pytest.mark.parametrize("B,T,K,N,dtype", [
-    (8, 1, 640, 4224, torch.bfloat16),     # few queries: split lists, partials in the scratch
+    (8, 1, 640, 4224, torch.bfloat16),     # few queries: split lists merged inside a cluster
     (2, 100, 300, 700, torch.float32),     # enough queries for whole lists per CTA
 ])
 def test_noalloc_matches_workspace_entry_two_calls(B, T, K, N, dtype):
