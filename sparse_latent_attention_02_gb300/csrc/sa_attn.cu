@@ -16,17 +16,19 @@
 //     The chunk sits in shared memory once, 128-byte swizzled; it is the
 //     K-major A operand of the first product and the MN-major A operand of
 //     the second.  Q (64 KB) stays resident for the whole segment.
-//   * Warp roles (24 warps): warps 0-3 softmax + epilogue (thread i owns
-//     TMEM lane i = chunk row i during the softmax, output feature
-//     128*tile + i in the epilogue); warps 4-19 gather the rows with 16-byte
-//     cp.async straight into the swizzled layout (an SM needs about sixteen
-//     warps of outstanding copies to draw ~40 B/clk of scattered rows from
-//     L2; a single TMA-issuing thread or warp reaches ~6 B/clk); warp 20
-//     compacts each index list into a double-buffered shared list, loads Q
-//     by TMA and, when kv is larger than L2, warms L2 with the next
-//     segment's rows; warp 21 allocates TMEM and issues the MMAs (one
-//     elected lane).  setmaxnreg gives the softmax warpgroup 240 registers
-//     per thread and every other warp 48.
+//   * Warp roles (28 warps): warps 0-7 softmax + epilogue (two warps per
+//     TMEM lane quarter, each with 32 of the 64 heads: a thread owns chunk
+//     row 32*(w%4) + lane during the softmax and that output feature of
+//     each 128-feature tile in the epilogue); warps 8-23 gather the rows
+//     with 16-byte cp.async straight into the swizzled layout (an SM needs
+//     about sixteen warps of outstanding copies to draw ~40 B/clk of
+//     scattered rows from L2; a single TMA-issuing thread or warp reaches
+//     ~6 B/clk); warp 24 loads Q by TMA, compacts each index list into a
+//     double-buffered shared list and, when kv is larger than L2, warms L2
+//     with the next segment's rows; warp 25 allocates TMEM and issues the
+//     MMAs (one elected lane); warps 26-27 only complete the last
+//     warpgroup.  setmaxnreg gives the softmax warps 152 registers per
+//     thread and every other warp 40.
 //   * Online softmax in base 2 with the sink as the starting maximum and a
 //     lazy rescale: the running maximum moves only when a score exceeds it by
 //     more than 2^8, so O^T in TMEM is almost never rewritten.  Row sums are
@@ -43,10 +45,23 @@ namespace sa {
 namespace attn {
 
 constexpr int H = 64, D = 512, CH = 128;
+constexpr int NUM_SOFTMAX_WARPS = 8;            // warps 0 .. 7: two per TMEM lane quarter
+constexpr int SMX_THREADS = NUM_SOFTMAX_WARPS * 32;
 constexpr int NUM_GATHER_WARPS = 16;
-constexpr int WARP_GATHER0 = 4;                 // warps 4 .. 19
-constexpr int WARP_CONTROL = 20, WARP_MMA = 21; // warps 22, 23 only lend registers
-constexpr int THREADS = 24 * 32;
+constexpr int WARP_GATHER0 = NUM_SOFTMAX_WARPS; // warps 8 .. 23
+constexpr int WARP_CONTROL = WARP_GATHER0 + NUM_GATHER_WARPS, WARP_MMA = WARP_CONTROL + 1;
+// setmaxnreg must be executed by every warp of a warpgroup: the block is whole
+// warpgroups (warps 26, 27 have no role and only lend registers).
+constexpr int THREADS = 28 * 32;                // 896
+// Register split (setmaxnreg): the launch gives every thread 72; the softmax
+// warps take 152 and the other 20 warps keep 40: 256*152 + 640*40 = 896*72.
+constexpr int REGS_SOFTMAX = 152, REGS_OTHER = 40, REGS_LAUNCH = 72;
+static_assert(THREADS % 128 == 0 && NUM_SOFTMAX_WARPS % 4 == 0, "setmaxnreg acts on whole warpgroups");
+static_assert(THREADS >= (WARP_MMA + 1) * 32, "every role has a warp");
+static_assert(REGS_LAUNCH * THREADS <= 65536 && (65536 / THREADS) / 8 * 8 == REGS_LAUNCH,
+              "launch register count");
+static_assert(SMX_THREADS * REGS_SOFTMAX + (THREADS - SMX_THREADS) * REGS_OTHER <= THREADS * REGS_LAUNCH,
+              "register split exceeds the launch allocation");
 constexpr int MAX_CLUSTER = 8;                                // list pieces of one query
 constexpr int GATHER_GROUP_WARPS = NUM_GATHER_WARPS / 2;          // each group owns two tiles
 constexpr int ROWS_PER_GATHER_WARP = CH / GATHER_GROUP_WARPS;     // 16
@@ -92,7 +107,7 @@ enum : uint32_t {
     B_XFULL,     // split schedule: every peer's partial for this CTA's heads has arrived (bytes)
     NUM_BARS
 };
-constexpr uint32_t LEMPTY_ARRIVALS = NUM_GATHER_WARPS + 1 + 4;   // gather warps, MMA, softmax warps
+constexpr uint32_t LEMPTY_ARRIVALS = NUM_GATHER_WARPS + 1 + NUM_SOFTMAX_WARPS;   // gather warps, MMA, softmax warps
 static_assert(NUM_BARS <= 32, "barrier area");
 
 constexpr uint32_t TMEM_COLS = 512, TM_S = 0, TM_O = 256;
@@ -218,31 +233,24 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     }
 }
 
-// Reduce 64 per-thread values over the 32 lanes of a warp with 62 shuffles:
-// each step halves the values a lane keeps.  On return v[0], v[1] hold the
-// warp-wide result for heads head0 and head0 + 1.
+// Reduce 32 per-thread values over the 32 lanes of a warp with 31 shuffles:
+// each step halves the values a lane keeps.  Returns the warp-wide result for
+// value index `lane`.
 template <bool MAX>
-__device__ __forceinline__ void warp_reduce64(float (&v)[64], int lane, int &head0)
+__device__ __forceinline__ float warp_reduce32(float (&v)[32], int lane)
 {
-#define SA_RED_STEP(W, BIT)                                                      \
-    {                                                                            \
-        const bool up = (lane & (BIT)) != 0;                                     \
-        _Pragma("unroll") for (int i = 0; i < (W); ++i)                          \
-        {                                                                        \
-            const float keep = up ? v[i + (W)] : v[i];                           \
-            const float send = up ? v[i] : v[i + (W)];                           \
-            const float got = __shfl_xor_sync(0xffffffffu, send, (BIT));         \
-            v[i] = MAX ? fmaxf(keep, got) : keep + got;                          \
-        }                                                                        \
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float keep = up ? v[i + w] : v[i];
+            const float send = up ? v[i] : v[i + w];
+            const float got = __shfl_xor_sync(0xffffffffu, send, w);
+            v[i] = MAX ? fmaxf(keep, got) : keep + got;
+        }
     }
-    SA_RED_STEP(32, 16)
-    SA_RED_STEP(16, 8)
-    SA_RED_STEP(8, 4)
-    SA_RED_STEP(4, 2)
-    SA_RED_STEP(2, 1)
-#undef SA_RED_STEP
-    head0 = ((lane & 16) ? 32 : 0) + ((lane & 8) ? 16 : 0) + ((lane & 4) ? 8 : 0) +
-            ((lane & 2) ? 4 : 0) + ((lane & 1) ? 2 : 0);
+    return v[0];
 }
 
 // ------------------------------------------------------------------ roles
@@ -267,7 +275,7 @@ __device__ __forceinline__ bool load_q(const AttnParams &p, uint32_t sbase, cons
     return true;
 }
 
-// Warp 20: loads every segment's Q by TMA and its index list into the
+// Warp 24: loads every segment's Q by TMA and its index list into the
 // staging buffer, compacts the list into a double-buffered shared list and
 // publishes its length.  When kv is larger than L2 it then warms L2 with the
 // next segment's rows while the current segment is processed.
@@ -336,7 +344,7 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     __syncwarp();
 }
 
-// Warps 4-19: gather the compacted rows, chunk by chunk, in two groups of
+// Warps 8-23: gather the compacted rows, chunk by chunk, in two groups of
 // eight warps: group g fills tiles g and g + 2 (a tile is two 64-feature
 // slices of the 128 rows), so all four tiles of a chunk can be in flight at
 // once and each tile is refilled as soon as the PV product frees it.  Warp w
@@ -425,7 +433,7 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
     __syncwarp();
 }
 
-// Lane 0 of warp 21 runs this role alone: the tensor pipe reaches its rate
+// Lane 0 of warp 25 runs this role alone: the tensor pipe reaches its rate
 // only when MMAs are issued back to back, so the issuing thread avoids warp
 // divergence and keeps its descriptor arithmetic to one add per MMA (the
 // start-address field, address >> 4, is the low 14 bits of a descriptor).
@@ -540,10 +548,11 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 //   M = max_r m_r (each m_r starts at the sink),  w_r = 2^(m_r - M),
 //   o = sum_r w_r O_r / (sum_r w_r l_r + 2^(sink*log2e - M))
 // then applies the inverse RoPE when asked and writes its heads.  Softmax
-// warpgroup only (thread t = TMEM lane t); false when a wait ran out.
+// warps only: warp (quarter qd, half hf) handles features 128d + 32qd + lane
+// of tiles d = 2hf, 2hf + 1.  False when a wait ran out.
 template <int P>
 __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl, const Seg &s,
-                              int nc, int t, volatile int *abort_flag, int lane)
+                              int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
 {
     constexpr int HP = H / P;
     constexpr uint32_t SLOT_BYTES = HP * D * 4;      // one piece's O for HP heads, [HP][512] fp32
@@ -557,13 +566,14 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     const float *recv = reinterpret_cast<const float *>(smem + OFF_KV);   // [P][HP][512] fp32
     float *stage = reinterpret_cast<float *>(smem + OFF_KV + me * SLOT_BYTES);
     float *xsend = reinterpret_cast<float *>(smem + OFF_XSEND);
+    const int fl = 32 * qd + lane;   // feature within a 128-feature tile
 
     if (t == 0)
         mbar_arrive_expect_tx(bar0 + 8 * B_XFULL, (P - 1) * (SLOT_BYTES + STAT_BYTES));
     if (t < P && t != (int)me)
         mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
     bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
-    if (bar_red_or(1, 128, !ok || *abort_flag))
+    if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
         return false;
 
     // send: peer g gets columns g*HP .. g*HP + HP-1 of every 128-feature tile
@@ -575,15 +585,16 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             // the previous copy has finished reading the staging slot
             if (t == 0)
                 bulk_wait_read_all();
-            bar_sync(1, 128);
+            bar_sync(1, SMX_THREADS);
         }
         first = false;
         if (t < HP) {
             xsend[t] = m_s[g * HP + t];
             xsend[HP + t] = lt[g * HP + t];
         }
-#pragma unroll 1
-        for (int d = 0; d < 4; ++d) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int d = 2 * hf + e;
             uint32_t v[HP];
             if (nc > 0) {
 #pragma unroll
@@ -597,10 +608,10 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             }
 #pragma unroll
             for (int i = 0; i < HP; ++i)
-                stage[i * D + 128 * d + t] = __uint_as_float(v[i]);
+                stage[i * D + 128 * d + fl] = __uint_as_float(v[i]);
         }
         fence_proxy_async_smem();
-        bar_sync(1, 128);
+        bar_sync(1, SMX_THREADS);
         if (t == 0) {
             const uint32_t rbar = mapa_shared(bar0 + 8 * B_XFULL, (uint32_t)g);
             bulk_copy_to_peer(mapa_shared(sbase + OFF_KV + me * SLOT_BYTES, (uint32_t)g),
@@ -614,7 +625,7 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         bulk_wait_read_all();
 
     ok = warp_wait_cluster(bar0 + 8 * B_XFULL, 0, abort_flag, p.timeout_ns, lane);
-    if (bar_red_or(1, 128, !ok || *abort_flag))
+    if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
         return false;
 
     if (t < HP) {
@@ -637,12 +648,14 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         den += M == -INFINITY ? 0.f : ex2(sl - M);
         wts[P * HP + t] = den > 0.f ? 1.f / den : 0.f;
     }
-    bar_sync(1, 128);
+    bar_sync(1, SMX_THREADS);
 
-    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
+    // each half stages its tile as [HP heads][128 features] bf16 in its half of the P buffer
+    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P) + hf * (HP * 128);
 #pragma unroll 1
-    for (int d = 0; d < 4; ++d) {
-        const int f = 128 * d + t;
+    for (int e = 0; e < 2; ++e) {
+        const int d = 2 * hf + e;
+        const int f = 128 * d + fl;
         uint32_t v[HP];
         if (nc > 0) {
 #pragma unroll
@@ -686,34 +699,42 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             for (int i = 0; i < HP; ++i)
                 po[i * D] = o[i];
         } else {
-            // stage [HP heads][128 features] bf16, then write 256-byte head rows with 16-byte stores
 #pragma unroll
             for (int i = 0; i < HP; ++i)
-                stg[i * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(o[i]));
-            bar_sync(1, 128);
+                stg[i * 128 + fl] = __bfloat16_as_ushort(__float2bfloat16_rn(o[i]));
+            bar_sync(2 + hf, 128);
+            // 256-byte head rows of this tile with 16-byte stores
+            const int tt = t & 127;
             uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + (size_t)(me * HP) * D + 128 * d) * 2;
+            const uint8_t *sp = reinterpret_cast<const uint8_t *>(stg);
 #pragma unroll
             for (int j = 0; j < HP / 8; ++j) {
-                const int c = t + 128 * j;   // 16-byte piece c: head c / 16, part c % 16
+                const int c = tt + 128 * j;   // 16-byte piece c: head c / 16, part c % 16
                 const int h = c >> 4, part = c & 15;
-                const uint4 val = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
+                const uint4 val = *reinterpret_cast<const uint4 *>(sp + h * 256 + part * 16);
                 *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = val;
             }
-            bar_sync(1, 128);
+            bar_sync(2 + hf, 128);
         }
     }
     return true;
 }
 
+// Warps 0-7: softmax and epilogue.  Warp w reads TMEM lane quarter qd = w % 4
+// (chunk rows 32qd .. 32qd + 31, one per thread) and owns heads
+// 32hf .. 32hf + 31, hf = w / 4.
 __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tmem,
                              int warp, int lane, volatile int *abort_flag)
 {
-    const int t = threadIdx.x;   // 0..127
-    float *red = reinterpret_cast<float *>(smem + OFF_RED);
+    const int t = threadIdx.x;   // 0..255
+    const int qd = warp & 3, hf = warp >> 2;
+    const int row = 32 * qd + lane;
+    const int hb = 32 * hf;      // first head of this thread
+    float *red = reinterpret_cast<float *>(smem + OFF_RED);   // [4 quarters][64 heads]
     float *m_s = reinterpret_cast<float *>(smem + OFF_M);
     float *aux = reinterpret_cast<float *>(smem + OFF_AUX);
     const uint32_t bar0 = sbase + OFF_BAR;
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's TMEM lane quarter
+    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);   // this warp's TMEM lane quarter
     const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
     uint32_t ph_sfull = 0, ph_pvdone = 0, ph_lfull[2] = {0, 0};
     SegIter it;
@@ -724,7 +745,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         const bool w0 = warp_wait(bar0 + 8 * (B_LFULL0 + b), ph_lfull[b], abort_flag, p.timeout_ns, lane);
         ph_lfull[b] ^= 1u;
         // also: the previous epilogue is done with m_s / aux
-        if (bar_red_or(1, 128, !w0 || *abort_flag))
+        if (bar_red_or(1, SMX_THREADS, !w0 || *abort_flag))
             break;
         const int n = segn[b];
         __syncwarp();
@@ -734,12 +755,12 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
 
         if (t < 64)
             m_s[t] = __ldg(p.sink + t) * LOG2E;
-        bar_sync(1, 128);
+        bar_sync(1, SMX_THREADS);
 
-        float l[64];
+        float l[32];
 #pragma unroll
-        for (int h = 0; h < 64; ++h)
-            l[h] = 0.f;
+        for (int i = 0; i < 32; ++i)
+            l[i] = 0.f;
 
         bool aborted = false;
         for (int c = 0; c < nc; ++c) {
@@ -753,31 +774,27 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 ph_pvdone ^= 1u;
             }
             tc_fence_after();
-            uint32_t r[64];
-            tmem_ld32(tl + TM_S, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-            tmem_ld32(tl + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+            uint32_t r[32];
+            tmem_ld32(tl + TM_S + hb, r);
             tmem_wait_ld();
-            const bool vrow = c * CH + t < n;
-            float x[64];
+            const bool vrow = c * CH + row < n;
+            float x[32];
             bool need = false;
 #pragma unroll
-            for (int h = 0; h < 64; ++h) {
-                x[h] = vrow ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
-                need |= x[h] > m_s[h] + RESCALE_THRESHOLD;
+            for (int i = 0; i < 32; ++i) {
+                x[i] = vrow ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                need |= x[i] > m_s[hb + i] + RESCALE_THRESHOLD;
             }
             // one barrier in the common case: it carries the rescale vote and
             // any failed wait; a second one tells the two apart
-            if (bar_red_or(1, 128, need || !wok || *abort_flag)) {
-                if (bar_red_or(1, 128, !wok || *abort_flag)) {
+            if (bar_red_or(1, SMX_THREADS, need || !wok || *abort_flag)) {
+                if (bar_red_or(1, SMX_THREADS, !wok || *abort_flag)) {
                     aborted = true;
                     break;
                 }
                 // move the running maximum to this chunk's maximum (per head)
-                int h0;
-                warp_reduce64<true>(x, lane, h0);
-                red[warp * 64 + h0] = x[0];
-                red[warp * 64 + h0 + 1] = x[1];
-                bar_sync(1, 128);
+                red[qd * 64 + hb + lane] = warp_reduce32<true>(x, lane);
+                bar_sync(1, SMX_THREADS);
                 if (t < 64) {
                     const float mx = fmaxf(fmaxf(red[t], red[64 + t]), fmaxf(red[128 + t], red[192 + t]));
                     const float mo = m_s[t];
@@ -785,50 +802,49 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                     aux[t] = ex2(mo - mn);
                     m_s[t] = mn;
                 }
-                bar_sync(1, 128);
+                bar_sync(1, SMX_THREADS);
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    l[h] *= aux[h];
+                for (int i = 0; i < 32; ++i)
+                    l[i] *= aux[hb + i];
                 if (c > 0) {
 #pragma unroll 1
                     for (int d = 0; d < 4; ++d) {
-#pragma unroll 1
-                        for (int hh = 0; hh < 2; ++hh) {
-                            uint32_t o[32];
-                            const uint32_t ta = tl + TM_O + 64 * d + 32 * hh;
-                            tmem_ld32(ta, o);
-                            tmem_wait_ld();
+                        uint32_t o[32];
+                        const uint32_t ta = tl + TM_O + 64 * d + hb;
+                        tmem_ld32(ta, o);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                o[i] = __float_as_uint(__uint_as_float(o[i]) * aux[32 * hh + i]);
-                            tmem_st32(ta, o);
-                        }
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * aux[hb + i]);
+                        tmem_st32(ta, o);
                     }
                     tmem_wait_st();
                 }
                 // x was consumed by the reduction: rebuild it from S^T
-                tmem_ld32(tl + TM_S, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_ld32(tl + TM_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_ld32(tl + TM_S + hb, r);
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 64; ++h)
-                    x[h] = vrow ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
+                for (int i = 0; i < 32; ++i)
+                    x[i] = vrow ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
             }
             // probabilities in bf16 (the MMA operand) and their row sums
-            uint32_t pk[32];
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float p0 = ex2(x[2 * i] - m_s[2 * i]);
-                const float p1 = ex2(x[2 * i + 1] - m_s[2 * i + 1]);
+            for (int i = 0; i < 16; ++i) {
+                const float p0 = ex2(x[2 * i] - m_s[hb + 2 * i]);
+                const float p1 = ex2(x[2 * i + 1] - m_s[hb + 2 * i + 1]);
                 pk[i] = pack_bf16x2(p0, p1);
                 l[2 * i] += bf16lo_to_f32(pk[i]);
                 l[2 * i + 1] += bf16hi_to_f32(pk[i]);
             }
-            uint8_t *prow = smem + OFF_P + t * 128;
+            // P^T row `row`: 64 heads x bf16 = 128 bytes, 16-byte chunks swizzled
+            uint8_t *prow = smem + OFF_P + row * 128;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (t & 7)) << 4)) =
-                    make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+            for (int j = 0; j < 4; ++j) {
+                const int c8 = 4 * hf + j;
+                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (row & 7)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar0 + 8 * B_PFULL);
@@ -838,19 +854,14 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         if (nc > 0) {
             const bool w = warp_wait(bar0 + 8 * B_PVDONE, ph_pvdone, abort_flag, p.timeout_ns, lane);
             ph_pvdone ^= 1u;
-            if (bar_red_or(1, 128, !w || *abort_flag))
+            if (bar_red_or(1, SMX_THREADS, !w || *abort_flag))
                 break;
             tc_fence_after();
         }
 
-        // row sums: reduce the per-row partials over the 128 threads
-        {
-            int h0;
-            warp_reduce64<false>(l, lane, h0);
-            red[warp * 64 + h0] = l[0];
-            red[warp * 64 + h0 + 1] = l[1];
-        }
-        bar_sync(1, 128);
+        // row sums: reduce the per-row partials over the rows of each warp, then the quarters
+        red[qd * 64 + hb + lane] = warp_reduce32<false>(l, lane);
+        bar_sync(1, SMX_THREADS);
         if (t < 64) {
             const float lt = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
             if (s.full) {
@@ -860,14 +871,14 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 aux[t] = lt;
             }
         }
-        bar_sync(1, 128);
+        bar_sync(1, SMX_THREADS);
 
         if (!s.full) {
             bool mok = false;
             switch (p.pieces) {
-            case 2: mok = cluster_merge<2>(p, smem, sbase, tl, s, nc, t, abort_flag, lane); break;
-            case 4: mok = cluster_merge<4>(p, smem, sbase, tl, s, nc, t, abort_flag, lane); break;
-            case 8: mok = cluster_merge<8>(p, smem, sbase, tl, s, nc, t, abort_flag, lane); break;
+            case 2: mok = cluster_merge<2>(p, smem, sbase, tl, s, nc, t, qd, hf, abort_flag, lane); break;
+            case 4: mok = cluster_merge<4>(p, smem, sbase, tl, s, nc, t, qd, hf, abort_flag, lane); break;
+            case 8: mok = cluster_merge<8>(p, smem, sbase, tl, s, nc, t, qd, hf, abort_flag, lane); break;
             default: break;
             }
             if (!mok)
@@ -879,24 +890,22 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
             continue;
         }
 
-        // epilogue: thread t owns feature 128*d + t of every head; both 32-head
-        // halves of a tile are read from TMEM before one wait
+        // epilogue: thread (qd, lane, hf) owns feature 128d + 32qd + lane of heads hb .. hb + 31
         const bool rope_here = p.rope_dim > 0;
         uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
 #pragma unroll 1
         for (int d = 0; d < 4; ++d) {
-            const int dim = 128 * d + t;
-            uint32_t u[64];
+            const int dim = 128 * d + row;
+            uint32_t u[32];
             if (nc > 0) {
-                tmem_ld32(tl + TM_O + 64 * d, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-                tmem_ld32(tl + TM_O + 64 * d + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+                tmem_ld32(tl + TM_O + 64 * d + hb, u);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    u[i] = __float_as_uint(__uint_as_float(u[i]) * aux[i]);
+                for (int i = 0; i < 32; ++i)
+                    u[i] = __float_as_uint(__uint_as_float(u[i]) * aux[hb + i]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
+                for (int i = 0; i < 32; ++i)
                     u[i] = 0u;
             }
             if (rope_here && dim >= D - p.rope_dim) {   // warp-uniform
@@ -905,34 +914,34 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 const float cth = __ldg(cs), sth = __ldg(cs + 1);
                 const bool odd = dim & 1;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                for (int i = 0; i < 32; ++i) {
                     const float o = __uint_as_float(u[i]);
                     const float other = __shfl_xor_sync(0xffffffffu, o, 1);
                     u[i] = __float_as_uint(odd ? (o * cth - other * sth) : (o * cth + other * sth));
                 }
             }
             if (p.out_f32) {
-                float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + dim;
+                float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + (size_t)hb * D + dim;
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    po[i * 512] = __uint_as_float(u[i]);
+                for (int i = 0; i < 32; ++i)
+                    po[i * D] = __uint_as_float(u[i]);
             } else {
                 // stage the tile as [64 heads][128 features] bf16 in the P buffer
                 // (free once the last PV is done), then write whole 256-byte head
                 // rows with 16-byte stores
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    stg[i * 128 + t] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[i])));
-                bar_sync(1, 128);
+                for (int i = 0; i < 32; ++i)
+                    stg[(hb + i) * 128 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[i])));
+                bar_sync(1, SMX_THREADS);
                 uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = t + 128 * i;   // 16-byte piece c: head c / 16, part c % 16
+                for (int j = 0; j < 4; ++j) {
+                    const int c = t + SMX_THREADS * j;   // 16-byte piece c: head c / 16, part c % 16
                     const int h = c >> 4, part = c & 15;
                     const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
                     *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
                 }
-                bar_sync(1, 128);
+                bar_sync(1, SMX_THREADS);
             }
         }
         if (nc > 0) {
@@ -961,9 +970,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             mbar_init(bar0 + 8 * (B_KVFREE0 + d), 1);
         }
         mbar_init(bar0 + 8 * B_SFULL, 1);
-        mbar_init(bar0 + 8 * B_PFULL, 128);
+        mbar_init(bar0 + 8 * B_PFULL, SMX_THREADS);
         mbar_init(bar0 + 8 * B_PVDONE, 1);
-        mbar_init(bar0 + 8 * B_OFREE, 128);
+        mbar_init(bar0 + 8 * B_OFREE, SMX_THREADS);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar0 + 8 * (B_LFULL0 + b), 32);
             mbar_init(bar0 + 8 * (B_LEMPTY0 + b), LEMPTY_ARRIVALS);
@@ -989,12 +998,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         cluster_sync();
     }
 
-    if (warp < 4) {
-        // the softmax warpgroup keeps 64 scores and 64 row sums per thread
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 240;" ::: "memory");
+    if (warp < NUM_SOFTMAX_WARPS) {
+        // the softmax warps keep 32 scores and 32 row sums per thread
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX) : "memory");
         softmax_role(p, smem, sbase, tmem, warp, lane, abort_flag);
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 48;" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_OTHER) : "memory");
         if (warp < WARP_GATHER0 + NUM_GATHER_WARPS)
             gather_role(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
         else if (warp == WARP_CONTROL)
