@@ -736,7 +736,8 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     const uint32_t bar0 = sbase + OFF_BAR;
     const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);   // this warp's TMEM lane quarter
     const int *segn = reinterpret_cast<const int *>(smem + OFF_SEGN);
-    uint32_t ph_sfull = 0, ph_pvdone = 0, ph_lfull[2] = {0, 0};
+    uint32_t ph_sfull = 0, ph_lfull[2] = {0, 0};
+    uint32_t chunks = 0;   // chunks processed so far: PV(j) is the (j+1)-th PVDONE completion
     SegIter it;
     seg_begin(p, it);
     Seg s;
@@ -764,15 +765,13 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
 
         bool aborted = false;
         for (int c = 0; c < nc; ++c) {
-            // S^T of this chunk is ready; PV of the previous chunk (issued before
-            // this chunk's QK) has then finished too, so P may be rewritten and
-            // O^T rescaled
-            bool wok = warp_wait(bar0 + 8 * B_SFULL, ph_sfull, abort_flag, p.timeout_ns, lane);
+            // S^T of this chunk is ready.  Its commit tracks every MMA issued
+            // before it, including the previous chunk's PV (issued before this
+            // chunk's QK): P may be rewritten and O^T rescaled without waiting
+            // for PVDONE.
+            const bool wok = warp_wait(bar0 + 8 * B_SFULL, ph_sfull, abort_flag, p.timeout_ns, lane);
             ph_sfull ^= 1u;
-            if (c > 0) {
-                wok = warp_wait(bar0 + 8 * B_PVDONE, ph_pvdone, abort_flag, p.timeout_ns, lane) && wok;
-                ph_pvdone ^= 1u;
-            }
+            ++chunks;
             tc_fence_after();
             uint32_t r[32];
             tmem_ld32(tl + TM_S + hb, r);
@@ -785,6 +784,16 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 x[i] = vrow ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
                 need |= x[i] > m_s[hb + i] + RESCALE_THRESHOLD;
             }
+            // probabilities in bf16 (the MMA operand) against the current maxima,
+            // computed before the vote so that the barrier absorbs the warps'
+            // skew; they are recomputed in the rare chunk that moves a maximum
+            uint32_t pk[16];
+            auto probabilities = [&]() {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(ex2(x[2 * i] - m_s[hb + 2 * i]), ex2(x[2 * i + 1] - m_s[hb + 2 * i + 1]));
+            };
+            probabilities();
             // one barrier in the common case: it carries the rescale vote and
             // any failed wait; a second one tells the two apart
             if (bar_red_or(1, SMX_THREADS, need || !wok || *abort_flag)) {
@@ -826,14 +835,11 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     x[i] = vrow ? __uint_as_float(r[i]) * p.scale_log2 : -INFINITY;
+                probabilities();
             }
-            // probabilities in bf16 (the MMA operand) and their row sums
-            uint32_t pk[16];
+            // row sums of the rounded probabilities
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float p0 = ex2(x[2 * i] - m_s[hb + 2 * i]);
-                const float p1 = ex2(x[2 * i + 1] - m_s[hb + 2 * i + 1]);
-                pk[i] = pack_bf16x2(p0, p1);
                 l[2 * i] += bf16lo_to_f32(pk[i]);
                 l[2 * i + 1] += bf16hi_to_f32(pk[i]);
             }
@@ -852,8 +858,9 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         if (aborted)
             break;
         if (nc > 0) {
-            const bool w = warp_wait(bar0 + 8 * B_PVDONE, ph_pvdone, abort_flag, p.timeout_ns, lane);
-            ph_pvdone ^= 1u;
+            // the segment's last PV: completion number `chunks`; every earlier
+            // one has completed (each chunk's S^T commit covered the PV before it)
+            const bool w = warp_wait(bar0 + 8 * B_PVDONE, (chunks - 1u) & 1u, abort_flag, p.timeout_ns, lane);
             if (bar_red_or(1, SMX_THREADS, !w || *abort_flag))
                 break;
             tc_fence_after();
