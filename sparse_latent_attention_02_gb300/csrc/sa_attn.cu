@@ -87,7 +87,8 @@ constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;        // [0] TMEM base, [1] abo
 constexpr uint32_t OFF_RAW = OFF_MISC + 64;           // int32 [SA_MAX_K] list as read from idx
 constexpr uint32_t OFF_XSTAT = OFF_RAW + 4 * SA_MAX_K;   // float [pieces][2][64 / pieces] peers' (m, l)
 constexpr uint32_t OFF_XSEND = OFF_XSTAT + 2 * 64 * 4;   // float [2][64 / pieces] (m, l) being sent
-constexpr uint32_t SMEM_USED = OFF_XSEND + 2 * 64 * 4;
+constexpr uint32_t OFF_SINK = OFF_XSEND + 2 * 64 * 4;    // float [64] sink * log2(e)
+constexpr uint32_t SMEM_USED = OFF_SINK + 64 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
@@ -557,6 +558,7 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     constexpr int HP = H / P;
     constexpr uint32_t SLOT_BYTES = HP * D * 4;      // one piece's O for HP heads, [HP][512] fp32
     constexpr uint32_t STAT_BYTES = 2 * HP * 4;      // its (m, l) for HP heads
+    constexpr int COPY_PARTS = 8;                    // a slot goes as 8 copies issued by 8 threads
     const uint32_t me = cluster_ctarank();
     const uint32_t bar0 = sbase + OFF_BAR;
     const float *m_s = reinterpret_cast<const float *>(smem + OFF_M);
@@ -583,7 +585,7 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             continue;
         if (!first) {
             // the previous copy has finished reading the staging slot
-            if (t == 0)
+            if (t < COPY_PARTS)
                 bulk_wait_read_all();
             bar_sync(1, SMX_THREADS);
         }
@@ -612,16 +614,17 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         }
         fence_proxy_async_smem();
         bar_sync(1, SMX_THREADS);
-        if (t == 0) {
+        if (t < COPY_PARTS) {
             const uint32_t rbar = mapa_shared(bar0 + 8 * B_XFULL, (uint32_t)g);
-            bulk_copy_to_peer(mapa_shared(sbase + OFF_KV + me * SLOT_BYTES, (uint32_t)g),
-                              sbase + OFF_KV + me * SLOT_BYTES, SLOT_BYTES, rbar);
-            bulk_copy_to_peer(mapa_shared(sbase + OFF_XSTAT + me * STAT_BYTES, (uint32_t)g),
-                              sbase + OFF_XSEND, STAT_BYTES, rbar);
+            const uint32_t off = OFF_KV + me * SLOT_BYTES + t * (SLOT_BYTES / COPY_PARTS);
+            bulk_copy_to_peer(mapa_shared(sbase + off, (uint32_t)g), sbase + off, SLOT_BYTES / COPY_PARTS, rbar);
+            if (t == 0)
+                bulk_copy_to_peer(mapa_shared(sbase + OFF_XSTAT + me * STAT_BYTES, (uint32_t)g),
+                                  sbase + OFF_XSEND, STAT_BYTES, rbar);
             bulk_commit();
         }
     }
-    if (t == 0)
+    if (t < COPY_PARTS)
         bulk_wait_read_all();
 
     ok = warp_wait_cluster(bar0 + 8 * B_XFULL, 0, abort_flag, p.timeout_ns, lane);
@@ -630,7 +633,7 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
 
     if (t < HP) {
         const int h = (int)me * HP + t;
-        const float sl = __ldg(p.sink + h) * LOG2E;
+        const float sl = reinterpret_cast<const float *>(smem + OFF_SINK)[h];
         float M = m_s[h];
 #pragma unroll
         for (int r = 0; r < P; ++r)
@@ -755,7 +758,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         const int nc = (n + CH - 1) / CH;
 
         if (t < 64)
-            m_s[t] = __ldg(p.sink + t) * LOG2E;
+            m_s[t] = reinterpret_cast<const float *>(smem + OFF_SINK)[t];
         bar_sync(1, SMX_THREADS);
 
         float l[32];
@@ -872,7 +875,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         if (t < 64) {
             const float lt = red[t] + red[64 + t] + red[128 + t] + red[192 + t];
             if (s.full) {
-                const float den = lt + ex2(__ldg(p.sink + t) * LOG2E - m_s[t]);
+                const float den = lt + ex2(reinterpret_cast<const float *>(smem + OFF_SINK)[t] - m_s[t]);
                 aux[t] = lt > 0.f ? 1.f / den : 0.f;
             } else {
                 aux[t] = lt;
@@ -991,6 +994,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);
     }
+    if (threadIdx.x < 64)
+        reinterpret_cast<float *>(smem + OFF_SINK)[threadIdx.x] = __ldg(p.sink + threadIdx.x) * LOG2E;
     if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
