@@ -38,8 +38,8 @@ HEADLINE = "decode"
 KERNEL_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)),
                           "sparse_latent_attention_02_gb300", "csrc", "sa_attn.cu")
 MEASURED_TRAFFIC = {
-    "decode": ("e3983699c30172913d57da63d3e73d02dec5c7dde27caf762ac3117df60edf19", 47_471_360),
-    "prefill": ("e3983699c30172913d57da63d3e73d02dec5c7dde27caf762ac3117df60edf19", 1_056_722_432),
+    "decode": ("f14d7d619332aff2905de859c228c655c254f5f0d9e30e1f67c898a48e9ae836", 47_189_504),
+    "prefill": ("f14d7d619332aff2905de859c228c655c254f5f0d9e30e1f67c898a48e9ae836", 1_058_844_672),
 }
 
 
