@@ -72,7 +72,13 @@ size_t sa_sparse_attn_workspace_size(int B, int T, int H, int D, int K);
  * sparse_attn ("DeepSeek-V4.1 > Output projection" page, Attention.forward).
  *   q      bf16 [B, T, H, D] contiguous, 16-byte aligned
  *   kv     bf16 [B, N, D] contiguous, 16-byte aligned: per batch row the
- *          window ring rows followed by the compressed rows
+ *          window ring rows followed by the compressed rows.  Device memory,
+ *          or page-locked host memory registered with CUDA (cudaHostAlloc,
+ *          cudaHostRegister): then the kernel gathers only the rows the
+ *          lists name straight from host memory over the CPU-GPU link, and
+ *          the rest of kv never moves.  Any other pointer (pageable host
+ *          memory, unknown) returns SA_ERR_INVALID_ARG before anything is
+ *          enqueued.  Every other buffer is device memory.
  *   sink   fp32 [H]
  *   idx    int32 [B, T, K] contiguous; values in [0, N) or -1 (skip)
  *   scale  softmax scale applied to q.k (the pages use D ** -0.5)

@@ -81,15 +81,16 @@ def _check(code: int, where: str):
         raise SAError(code, where)
 
 
-def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+def _need(t: torch.Tensor, name: str, dtype, ndim: int, pinned_ok: bool = False):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_cuda and not (pinned_ok and t.is_pinned()):
+        raise ValueError(f"{name} must live on a CUDA device"
+                         + (" or in page-locked host memory" if pinned_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
 
@@ -122,7 +123,8 @@ def fused_workspace_size(B: int, T: int, K: int, G: int, R: int) -> int:
 
 def _attn_args(q, kv, sink, idx):
     _need(q, "q", torch.bfloat16, 4)
-    _need(kv, "kv", torch.bfloat16, 3)
+    # kv may stay in page-locked host memory: the kernel gathers its rows from there
+    _need(kv, "kv", torch.bfloat16, 3, pinned_ok=True)
     _need(sink, "sink", torch.float32, 1)
     _need(idx, "idx", torch.int32, 3)
     B, T, H, D = q.shape
@@ -130,9 +132,9 @@ def _attn_args(q, kv, sink, idx):
         raise ValueError(f"kv {tuple(kv.shape)} does not match q {tuple(q.shape)}")
     if sink.shape[0] != H or idx.shape[:2] != (B, T):
         raise ValueError("sink / idx shapes do not match q")
-    devs = {t.device for t in (q, kv, sink, idx)}
+    devs = {t.device for t in (q, sink, idx)} | ({kv.device} if kv.is_cuda else set())
     if len(devs) != 1:
-        raise ValueError("all inputs must be on one device")
+        raise ValueError("all device inputs must be on one device")
     return B, T, H, D, kv.shape[1], idx.shape[2]
 
 

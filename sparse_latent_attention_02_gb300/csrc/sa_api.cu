@@ -39,6 +39,35 @@ bool current_sms(int *sms)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// kv may live in device (or managed) memory, or in page-locked host memory
+// registered with CUDA: then its device address is used and the kernel
+// gathers the rows it needs straight from host memory over the CPU-GPU link.
+// Anything else (pageable host memory, unknown pointers) is refused here,
+// before anything is enqueued.
+sa_status resolve_kv(const void *kv, const void **dev_kv, bool *host)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, kv) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SA_ERR_INVALID_ARG;
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+        *dev_kv = kv;
+        *host = false;
+        return SA_OK;
+    case cudaMemoryTypeHost:
+        if (!a.devicePointer)
+            return SA_ERR_INVALID_ARG;
+        *dev_kv = a.devicePointer;
+        *host = true;
+        return SA_OK;
+    default:
+        return SA_ERR_INVALID_ARG;
+    }
+}
+
 sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const float *sink,
                            const int32_t *idx, float scale, int B, int T, int N, int K, void *out,
                            bool out_f32, void *ws)
@@ -47,13 +76,17 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const f
     const uint64_t rows = (uint64_t)B * T * SA_HEADS;
     if (!encode_tmap_2d(&p.tm_q, q, rows, SA_HEAD_DIM, 64, 64))
         return SA_ERR_CUDA;
-    // kv rows for four-row gathers (box one row high); with N == 0 nothing is
-    // gathered and the map is left empty
-    if (N > 0 && !encode_tmap_2d(&p.tm_kv, kv, (uint64_t)B * N, SA_HEAD_DIM, 64, 1))
-        return SA_ERR_CUDA;
-    // warm L2 with upcoming rows only when kv cannot stay resident in it
-    p.prefetch_rows = (uint64_t)B * N * SA_HEAD_DIM * 2 > ((uint64_t)96 << 20) ? 1 : 0;
-    p.kv = static_cast<const uint16_t *>(kv);
+    const void *dev_kv = kv;
+    bool host_kv = false;
+    if ((int64_t)B * T > 0 && K > 0 && N > 0) {
+        const sa_status st = resolve_kv(kv, &dev_kv, &host_kv);
+        if (st != SA_OK)
+            return st;
+    }
+    // warm L2 with upcoming rows only when kv lives in device memory too large
+    // to stay resident in L2
+    p.prefetch_rows = !host_kv && (uint64_t)B * N * SA_HEAD_DIM * 2 > ((uint64_t)96 << 20) ? 1 : 0;
+    p.kv = static_cast<const uint16_t *>(dev_kv);
     p.idx = idx;
     p.sink = sink;
     p.out = out;

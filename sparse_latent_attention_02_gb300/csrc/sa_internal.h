@@ -18,8 +18,7 @@ constexpr size_t WS_HEADER = 256;
 
 struct AttnParams {
     CUtensorMap tm_q;          // q as 2-D [B*T*H rows, D cols] bf16, box 64x64, 128B swizzle
-    CUtensorMap tm_kv;         // kv as 2-D [B*N rows, D cols] bf16, box 64x1 (row gathers), 128B swizzle
-    const uint16_t *kv;        // bf16 [B, N, D]
+    const uint16_t *kv;        // bf16 [B, N, D]: device memory or page-locked host memory
     const int32_t *idx;        // int32 [B*T, K]
     const float *sink;         // fp32 [H]
     void *out;                 // [B*T, H, D] bf16 or fp32

@@ -222,3 +222,34 @@ def test_repeat_calls_are_deterministic():
     b = sa.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_kv_in_pinned_host_memory():
+    """kv left in page-locked host memory: the kernel gathers the listed rows
+    straight from there; the result is bit-identical to kv in device memory.
+    Pageable host memory is refused before anything is enqueued."""
+    g = torch.Generator().manual_seed(23)
+    for B, T, K, N in [(4, 1, 640, 1000), (1, 200, 300, 500)]:   # split and whole schedules
+        q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16)
+        kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16)
+        sink = torch.randn(64, generator=g)
+        idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
+        idx[torch.rand(B, T, K, generator=g) < 0.1] = -1
+        x = dict(q=q, kv=kv, sink=sink, idx=idx)
+        on_device = run(x, 512 ** -0.5, torch.float32)
+        gd = to_dev(x)
+        on_host = sa.sparse_attn(gd["q"], kv.pin_memory(), gd["sink"], gd["idx"], 512 ** -0.5,
+                                 out_dtype=torch.float32, check=True)
+        assert torch.equal(on_host, on_device), f"B{B} T{T}"
+        compare(on_host.double().cpu().numpy(), full_oracle(x, 512 ** -0.5), f"host kv B{B} T{T}")
+    # pageable memory: refused by the binding, and by the C ABI itself
+    pageable = kv.clone()
+    with pytest.raises(ValueError):
+        sa.sparse_attn(gd["q"], pageable, gd["sink"], gd["idx"], 0.1)
+    lib = sa.library()
+    out = torch.empty(1, T, 64, 512, dtype=torch.float32, device="cuda")
+    ws = sa._ws_cache[(torch.cuda.current_device(), "attn")]
+    code = lib.sa_sparse_attn(gd["q"].data_ptr(), pageable.data_ptr(), gd["sink"].data_ptr(),
+                              gd["idx"].data_ptr(), 0.1, 1, T, 64, 512, N, K, out.data_ptr(), 1,
+                              ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert code == 1   # SA_ERR_INVALID_ARG
