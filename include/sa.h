@@ -92,6 +92,33 @@ sa_status sa_sparse_attn(const void *q, const void *kv, const float *sink,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * sa_sparse_attn over the two latent sources of the "DeepSeek-V4.1 > Output
+ * projection" page's Attention.forward without concatenating them: the
+ * window ring (`window_kv_cache`, [max_batch, window, D]) and the compressed
+ * cache (`compress_kv_cache`, [max_batch, max_len / ratio, D]) that the page
+ * joins with torch.cat before calling sparse_attn.  The result is the same
+ * as sa_sparse_attn on kv = cat(window[:, :W], compressed[:, :C]) with N = W + C.
+ *   window_kv      bf16, row v < W of batch element b at
+ *                  window_kv + (b * window_bstride + v) * D; rows 16-byte aligned
+ *   W              rows of the window source per batch element (>= 0)
+ *   window_bstride batch stride of the window source, in rows (>= W)
+ *   compressed_kv  bf16, list index v >= W reads its row v - W of batch
+ *                  element b at compressed_kv + (b * compressed_bstride + v - W) * D
+ *   C, compressed_bstride  as for the window source
+ *   idx            int32 [B, T, K]; values in [0, W + C) or -1 (skip)
+ * Each source may be device memory or page-locked host memory (as kv of
+ * sa_sparse_attn); an unused source (W or C zero) may be NULL.  Other
+ * arguments, workspace and errors as for sa_sparse_attn.  Rows of a source
+ * beyond W or C (padding of a cache) are never read.
+ */
+sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W,
+                                    int64_t window_bstride, const void *compressed_kv,
+                                    int C, int64_t compressed_bstride, const float *sink,
+                                    const int32_t *idx, float scale, int B, int T, int H,
+                                    int D, int K, void *out, sa_dtype out_dtype,
+                                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Bytes of workspace `sa_sparse_attn_rope_wo_a` needs: the attention
  * workspace plus the bf16 attention output [B, T, H, D] it keeps between the
  * two steps.

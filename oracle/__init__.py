@@ -127,6 +127,25 @@ def sparse_attn(q, kv, sink, idx, scale: float, queries=None, n_threads: int = 0
     return out, int(bad)
 
 
+def sparse_attn_two_source(q, window_kv, W: int, compressed_kv, C: int, sink, idx, scale: float,
+                           queries=None, n_threads: int = 0):
+    """fp64 ``sparse_attn`` over the window ring and the compressed cache, as the
+    "DeepSeek-V4.1 > Output projection" page's Attention.forward builds its kv:
+    ``torch.cat([window_kv, compress_kv], dim=1)`` (first W window rows, then
+    the first C compressed rows of each batch element), then ``sparse_attn``.
+    window_kv / compressed_kv bf16 [>= B, >= W / >= C, D] (None when W / C is 0).
+    """
+    qb = _as_bf16_bits(q)
+    B, _, _, D = qb.shape
+    parts = []
+    if W:
+        parts.append(_as_bf16_bits(window_kv)[:B, :W])
+    if C:
+        parts.append(_as_bf16_bits(compressed_kv)[:B, :C])
+    kv = np.concatenate(parts, axis=1) if parts else np.zeros((B, 0, D), dtype=np.uint16)
+    return sparse_attn(qb, np.ascontiguousarray(kv), sink, idx, scale, queries=queries, n_threads=n_threads)
+
+
 def inverse_rope(o: np.ndarray, pos, rope_dim: int, theta: float, n_threads: int = 0):
     """In-place-free inverse rotary embedding of the last ``rope_dim`` features.
 

@@ -18,13 +18,13 @@ import torch
 
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
-__all__ = ["sparse_attn", "sparse_attn_rope_wo_a", "rope_table", "workspace_size",
+__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_rope_wo_a", "rope_table", "workspace_size",
            "fused_workspace_size", "check_errors", "SAError", "library", "build"]
 
 HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
 _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_WORKSPACE",
            4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA"}
-EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn",
+EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_two_source",
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc")
 
@@ -55,6 +55,10 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_sparse_attn_workspace_size.argtypes = [I, I, I, I, I]
             lib.sa_sparse_attn.restype = I
             lib.sa_sparse_attn.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, Z, V]
+            L = ctypes.c_int64
+            lib.sa_sparse_attn_two_source.restype = I
+            lib.sa_sparse_attn_two_source.argtypes = [V, V, I, L, V, I, L, V, V, F, I, I, I, I, I, V, I,
+                                                      V, Z, V]
             lib.sa_sparse_attn_rope_wo_a_workspace_size.restype = Z
             lib.sa_sparse_attn_rope_wo_a_workspace_size.argtypes = [I, I, I, I, I, I, I]
             lib.sa_sparse_attn_rope_wo_a.restype = I
@@ -163,6 +167,73 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torc
                               1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
                               workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check(code, "sa_sparse_attn")
+    if check:
+        check_errors(workspace, stream)
+    return out
+
+
+def _source(t: torch.Tensor | None, name: str, used: int | None, B: int, D: int):
+    """(pointer, used rows, batch stride in rows) of one latent source [Bmax, rows, D]."""
+    if t is None:
+        if used:
+            raise ValueError(f"{name} is missing")
+        return 0, 0, 0
+    _need_rows(t, name, D)
+    if t.shape[0] < B:
+        raise ValueError(f"{name} has {t.shape[0]} batch rows, q has {B}")
+    rows = t.shape[1] if used is None else int(used)
+    if not 0 <= rows <= t.shape[1]:
+        raise ValueError(f"{name}: {rows} rows used of {t.shape[1]}")
+    return t.data_ptr(), rows, t.stride(0) // D
+
+
+def _need_rows(t: torch.Tensor, name: str, D: int):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 3 or t.shape[2] != D:
+        raise TypeError(f"{name} must be a bf16 tensor [batch, rows, {D}]")
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must live on a CUDA device or in page-locked host memory")
+    if t.stride(2) != 1 or t.stride(1) != D or t.stride(0) % D:
+        raise ValueError(f"{name} must have contiguous {D}-element rows")
+
+
+def sparse_attn_two_source(q: torch.Tensor, window_kv: torch.Tensor | None,
+                           compressed_kv: torch.Tensor | None, sink: torch.Tensor, idx: torch.Tensor,
+                           scale: float, W: int | None = None, C: int | None = None,
+                           out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.bfloat16,
+                           workspace: torch.Tensor | None = None, stream=None,
+                           check: bool = False) -> torch.Tensor:
+    """sparse_attn over the window ring and the compressed cache read in place:
+    the same result as ``sparse_attn(q, cat(window_kv[:, :W], compressed_kv[:, :C], 1), ...)``.
+
+    window_kv bf16 [Bmax, >= W, 512] and compressed_kv bf16 [Bmax, >= C, 512] may be
+    views of larger caches (their batch strides are used); W and C default to
+    their row counts; idx values lie in [0, W + C) or are -1.
+    """
+    _need(q, "q", torch.bfloat16, 4)
+    _need(sink, "sink", torch.float32, 1)
+    _need(idx, "idx", torch.int32, 3)
+    B, T, H, D = q.shape
+    if sink.shape[0] != H or idx.shape[:2] != (B, T):
+        raise ValueError("sink / idx shapes do not match q")
+    pw, W, sw = _source(window_kv, "window_kv", W, B, D)
+    pc, C, sc = _source(compressed_kv, "compressed_kv", C, B, D)
+    K = idx.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=out_dtype, device=q.device)
+    else:
+        _need(out, "out", out.dtype, 4)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    lib = library()
+    need = int(lib.sa_sparse_attn_workspace_size(B, T, H, D, K))
+    if workspace is None:
+        workspace = _workspace(need, q.device, "attn")
+    code = lib.sa_sparse_attn_two_source(q.data_ptr(), pw, W, sw, pc, C, sc, sink.data_ptr(),
+                                         idx.data_ptr(), float(scale), B, T, H, D, K, out.data_ptr(),
+                                         1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_ptr(stream))
+    _check(code, "sa_sparse_attn_two_source")
     if check:
         check_errors(workspace, stream)
     return out

@@ -68,7 +68,18 @@ sa_status resolve_kv(const void *kv, const void **dev_kv, bool *host)
     }
 }
 
-sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const float *sink,
+// The latent rows come from one or two sources (see AttnParams): list index
+// v < W is row v of kv (batch stride kv_bstride rows), v >= W is row v - W of
+// kv2 (batch stride kv2_bstride rows); N = W + rows of kv2.
+struct KvSources {
+    const void *kv;
+    int64_t kv_bstride;
+    int W;
+    const void *kv2;
+    int64_t kv2_bstride;
+};
+
+sa_status fill_attn_params(AttnParams &p, const void *q, const KvSources &src, const float *sink,
                            const int32_t *idx, float scale, int B, int T, int N, int K, void *out,
                            bool out_f32, void *ws)
 {
@@ -76,17 +87,28 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const void *kv, const f
     const uint64_t rows = (uint64_t)B * T * SA_HEADS;
     if (!encode_tmap_2d(&p.tm_q, q, rows, SA_HEAD_DIM, 64, 64))
         return SA_ERR_CUDA;
-    const void *dev_kv = kv;
-    bool host_kv = false;
-    if ((int64_t)B * T > 0 && K > 0 && N > 0) {
-        const sa_status st = resolve_kv(kv, &dev_kv, &host_kv);
-        if (st != SA_OK)
-            return st;
+    const void *dev_kv = src.kv, *dev_kv2 = src.kv2;
+    bool host_kv = false, host_kv2 = false;
+    if ((int64_t)B * T > 0 && K > 0) {
+        if (src.W > 0) {
+            const sa_status st = resolve_kv(src.kv, &dev_kv, &host_kv);
+            if (st != SA_OK)
+                return st;
+        }
+        if (N > src.W) {
+            const sa_status st = resolve_kv(src.kv2, &dev_kv2, &host_kv2);
+            if (st != SA_OK)
+                return st;
+        }
     }
     // warm L2 with upcoming rows only when kv lives in device memory too large
     // to stay resident in L2
-    p.prefetch_rows = !host_kv && (uint64_t)B * N * SA_HEAD_DIM * 2 > ((uint64_t)96 << 20) ? 1 : 0;
+    p.prefetch_rows = !host_kv && !host_kv2 && (uint64_t)B * N * SA_HEAD_DIM * 2 > ((uint64_t)96 << 20) ? 1 : 0;
     p.kv = static_cast<const uint16_t *>(dev_kv);
+    p.kv2 = static_cast<const uint16_t *>(dev_kv2);
+    p.kv_bstride = src.kv_bstride;
+    p.kv2_bstride = src.kv2_bstride;
+    p.W = src.W;
     p.idx = idx;
     p.sink = sink;
     p.out = out;
@@ -200,7 +222,54 @@ sa_status sa_sparse_attn(const void *q, const void *kv, const float *sink, const
     if (K == 0)
         return cudaMemsetAsync(out, 0, (size_t)BT * H * D * esz, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
     AttnParams p;
-    st = fill_attn_params(p, q, kv, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
+    const KvSources src{kv, N, N, nullptr, 0};
+    st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
+    if (st != SA_OK)
+        return st;
+    const Schedule sch = attn_schedule(BT, K, sms);
+    return launch_attention(p, sch, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W, int64_t window_bstride,
+                                    const void *compressed_kv, int C, int64_t compressed_bstride,
+                                    const float *sink, const int32_t *idx, float scale, int B, int T, int H,
+                                    int D, int K, void *out, sa_dtype out_dtype, void *workspace,
+                                    size_t ws_bytes, void *stream)
+{
+    if (W < 0 || C < 0 || (int64_t)W + C >= ((int64_t)1 << 31))
+        return SA_ERR_INVALID_ARG;
+    const int N = W + C;
+    // the sources' own checks; kv itself is checked per source below
+    sa_status st = check_attn_args(q, W > 0 ? window_kv : compressed_kv, sink, idx, scale, B, T, H, D, N, K,
+                                   out, workspace);
+    if (st != SA_OK)
+        return st;
+    if (out_dtype != SA_BF16 && out_dtype != SA_F32)
+        return SA_ERR_INVALID_ARG;
+    const int64_t BT = (int64_t)B * T;
+    if (BT == 0)
+        return SA_OK;
+    if (K > 0) {
+        if (W > 0 && (!window_kv || !aligned(window_kv, 16) || window_bstride < W))
+            return SA_ERR_INVALID_ARG;
+        if (C > 0 && (!compressed_kv || !aligned(compressed_kv, 16) || compressed_bstride < C))
+            return SA_ERR_INVALID_ARG;
+        if ((int64_t)B * (W > 0 ? window_bstride : 0) >= ((int64_t)1 << 40) ||
+            (int64_t)B * (C > 0 ? compressed_bstride : 0) >= ((int64_t)1 << 40))
+            return SA_ERR_UNSUPPORTED;
+    }
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
+    if (ws_bytes < attn_workspace_bytes(BT, K, sms))
+        return SA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t esz = out_dtype == SA_F32 ? 4 : 2;
+    if (K == 0)
+        return cudaMemsetAsync(out, 0, (size_t)BT * H * D * esz, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+    AttnParams p;
+    const KvSources src{window_kv, window_bstride, W, compressed_kv, compressed_bstride};
+    st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
     if (st != SA_OK)
         return st;
     const Schedule sch = attn_schedule(BT, K, sms);
@@ -255,7 +324,8 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
             return SA_ERR_CUDA;
     } else {
         AttnParams p;
-        st = fill_attn_params(p, q, kv, sink, idx, scale, B, T, N, K, o, false, workspace);
+        const KvSources src{kv, N, N, nullptr, 0};
+        st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, o, false, workspace);
         if (st != SA_OK)
             return st;
         p.rope = rope_cos_sin;

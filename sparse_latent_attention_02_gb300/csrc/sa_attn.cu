@@ -27,8 +27,8 @@
 //     double-buffered shared list and, when kv is larger than L2, warms L2
 //     with the next segment's rows; warp 25 allocates TMEM and issues the
 //     MMAs (one elected lane); warps 26-27 only complete the last
-//     warpgroup.  setmaxnreg gives the softmax warps 152 registers per
-//     thread and every other warp 40.
+//     warpgroup.  setmaxnreg gives the softmax warps 128 registers per
+//     thread, the gather warps 48 and the last warpgroup 56.
 //   * Online softmax in base 2 with the sink as the starting maximum and a
 //     lazy rescale: the running maximum moves only when a score exceeds it by
 //     more than 2^8, so O^T in TMEM is almost never rewritten.  Row sums are
@@ -53,14 +53,18 @@ constexpr int WARP_CONTROL = WARP_GATHER0 + NUM_GATHER_WARPS, WARP_MMA = WARP_CO
 // setmaxnreg must be executed by every warp of a warpgroup: the block is whole
 // warpgroups (warps 26, 27 have no role and only lend registers).
 constexpr int THREADS = 28 * 32;                // 896
-// Register split (setmaxnreg): the launch gives every thread 72; the softmax
-// warps take 152 and the other 20 warps keep 40: 256*152 + 640*40 = 896*72.
-constexpr int REGS_SOFTMAX = 152, REGS_OTHER = 40, REGS_LAUNCH = 72;
+// Register split (setmaxnreg, per warpgroup): the launch gives every thread
+// 72; the softmax warps take 128, the gather warps keep 48 and the last
+// warpgroup (control, MMA) 56: 256*128 + 512*48 + 128*56 = 896*72.
+constexpr int REGS_SOFTMAX = 128, REGS_GATHER = 48, REGS_LAST = 56, REGS_LAUNCH = 72;
+constexpr int GATHER_THREADS = NUM_GATHER_WARPS * 32, LAST_THREADS = THREADS - SMX_THREADS - GATHER_THREADS;
 static_assert(THREADS % 128 == 0 && NUM_SOFTMAX_WARPS % 4 == 0, "setmaxnreg acts on whole warpgroups");
 static_assert(THREADS >= (WARP_MMA + 1) * 32, "every role has a warp");
 static_assert(REGS_LAUNCH * THREADS <= 65536 && (65536 / THREADS) / 8 * 8 == REGS_LAUNCH,
               "launch register count");
-static_assert(SMX_THREADS * REGS_SOFTMAX + (THREADS - SMX_THREADS) * REGS_OTHER <= THREADS * REGS_LAUNCH,
+static_assert(NUM_GATHER_WARPS % 4 == 0 && LAST_THREADS == 128, "one warpgroup after the gather warps");
+static_assert(SMX_THREADS * REGS_SOFTMAX + GATHER_THREADS * REGS_GATHER + LAST_THREADS * REGS_LAST <=
+                  THREADS * REGS_LAUNCH,
               "register split exceeds the launch allocation");
 constexpr int MAX_CLUSTER = 8;                                // list pieces of one query
 constexpr int GATHER_GROUP_WARPS = NUM_GATHER_WARPS / 2;          // each group owns two tiles
@@ -162,6 +166,20 @@ __device__ __forceinline__ bool seg_next(const AttnParams &p, SegIter &it, Seg &
     return s.q < p.BT;
 }
 
+// Latent row v (0 <= v < N) of batch element bidx.  One source: row v of kv.
+// Two sources (the window ring and the compressed cache of the pages, read in
+// place instead of concatenated): row v of source 0 when v < W, else row
+// v - W of source 1.  The kernel is built for each case, so that the one-source
+// gather keeps its single multiply-add per copy.
+template <bool TWO>
+__device__ __forceinline__ const uint16_t *kv_row(const AttnParams &p, int64_t bidx, int v)
+{
+    if (!TWO)
+        return p.kv + ((size_t)bidx * (size_t)p.kv_bstride + (size_t)v) * D;
+    return v < p.W ? p.kv + ((size_t)bidx * (size_t)p.kv_bstride + (size_t)v) * D
+                   : p.kv2 + ((size_t)bidx * (size_t)p.kv2_bstride + (size_t)(v - p.W)) * D;
+}
+
 // Start copying idx[q, j0:j1] into the staging buffer (whole warp, one
 // 4-byte cp.async per entry, all in flight at once: one memory round trip).
 __device__ __forceinline__ void stage_list(const AttnParams &p, const Seg &s, uint32_t raw, int lane)
@@ -201,15 +219,15 @@ __device__ __forceinline__ int compact_staged(const int32_t *raw, int len, int N
 
 // Warm L2 with latent rows (whole warp, one line prefetch per 128 bytes):
 // rows list[j0 .. j1) of batch element bidx, skipping entries outside [0, N).
+template <bool TWO>
 __device__ __forceinline__ void prefetch_rows(const AttnParams &p, int64_t bidx, const int32_t *list, int j0,
                                               int j1, int lane)
 {
-    const uint8_t *kvb = reinterpret_cast<const uint8_t *>(p.kv + (size_t)bidx * (size_t)p.N * D);
     // lane = 8 * (row within a group of 4) + line
     for (int j = j0 + (lane >> 3); j < j1; j += 4) {
         const int v = list[j];
         if (v >= 0 && v < p.N)
-            prefetch_l2_line(kvb + (size_t)v * (D * 2) + (lane & 7) * 128);
+            prefetch_l2_line(reinterpret_cast<const uint8_t *>(kv_row<TWO>(p, bidx, v)) + (lane & 7) * 128);
     }
 }
 
@@ -280,6 +298,7 @@ __device__ __forceinline__ bool load_q(const AttnParams &p, uint32_t sbase, cons
 // staging buffer, compacts the list into a double-buffered shared list and
 // publishes its length.  When kv is larger than L2 it then warms L2 with the
 // next segment's rows while the current segment is processed.
+template <bool TWO>
 __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int lane,
                              volatile int *abort_flag)
 {
@@ -333,7 +352,7 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
             if (p.prefetch_rows) {
                 cp_async_wait_all();
                 __syncwarp();
-                prefetch_rows(p, sn.q / p.T, raw, 0, sn.j1 - sn.j0, lane);
+                prefetch_rows<TWO>(p, sn.q / p.T, raw, 0, sn.j1 - sn.j0, lane);
             }
             s = sn;
         }
@@ -351,6 +370,7 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
 // once and each tile is refilled as soon as the PV product frees it.  Warp w
 // of a group copies rows 16w .. 16w+15; rows past the end of the list are
 // zero-filled.
+template <bool TWO>
 __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int gi, int lane,
                             volatile int *abort_flag)
 {
@@ -372,16 +392,22 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
         const int n = segn[b];
         const int32_t *cidx = reinterpret_cast<const int32_t *>(smem + OFF_IDX) + b * SA_MAX_K;
         const int nc = (n + CH - 1) / CH;
-        const uint16_t *kvb = p.kv + (size_t)(s.q / p.T) * (size_t)p.N * D;
+        const int64_t bidx = s.q / p.T;
+        // this batch element's rows in each source (the second only with two sources)
+        const uint16_t *kvb = p.kv + (size_t)bidx * (size_t)p.kv_bstride * D;
+        const uint16_t *kvb2 = TWO ? p.kv2 + ((size_t)bidx * (size_t)p.kv2_bstride - (size_t)p.W) * D : nullptr;
+        auto row_ptr = [&](int v) -> const uint16_t * {
+            return (TWO && v >= p.W) ? kvb2 + (size_t)v * D : kvb + (size_t)v * D;
+        };
         for (int c = 0; c < nc && ok; ++c) {
             const int rows = min(CH, n - c * CH);
-            // this lane's eight (row, 16-byte piece) jobs; the rows are the same for both tiles
-            int r[8], row[8];
+            // this lane's eight (row, 16-byte piece) jobs, rows r0 + 2i; the rows
+            // are the same for both tiles
+            const int r0 = ROWS_PER_GATHER_WARP * wg + (lane >> 4);
+            int row[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                r[i] = ROWS_PER_GATHER_WARP * wg + 2 * i + (lane >> 4);
-                row[i] = r[i] < rows ? cidx[c * CH + r[i]] : -1;
-            }
+            for (int i = 0; i < 8; ++i)
+                row[i] = r0 + 2 * i < rows ? cidx[c * CH + r0 + 2 * i] : -1;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int d = grp + 2 * e;
@@ -392,8 +418,9 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                 const int sl = 2 * d + (pc >> 3), ch = pc & 7;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r[i] * 128 + ((ch ^ (r[i] & 7)) << 4);
-                    const uint16_t *src = kvb + (size_t)(row[i] < 0 ? 0 : row[i]) * D + sl * 64 + ch * 8;
+                    const int r = r0 + 2 * i;
+                    const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r * 128 + ((ch ^ (r & 7)) << 4);
+                    const uint16_t *src = row_ptr(row[i] < 0 ? 0 : row[i]) + sl * 64 + ch * 8;
                     cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
                 }
                 cp_async_commit();
@@ -417,7 +444,7 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
             if (p.prefetch_rows && c + 1 < nc) {
                 const int j = (c + 1) * CH + ROWS_PER_GATHER_WARP * wg + (lane >> 1);
                 if (j < n) {
-                    const uint8_t *rp = reinterpret_cast<const uint8_t *>(kvb + (size_t)cidx[j] * D) +
+                    const uint8_t *rp = reinterpret_cast<const uint8_t *>(row_ptr(cidx[j])) +
                                         (grp + 2 * (lane & 1)) * 256;
                     prefetch_l2_line(rp);
                     prefetch_l2_line(rp + 128);
@@ -961,6 +988,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     }
 }
 
+template <bool TWO>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ AttnParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -1014,12 +1042,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         // the softmax warps keep 32 scores and 32 row sums per thread
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_SOFTMAX) : "memory");
         softmax_role(p, smem, sbase, tmem, warp, lane, abort_flag);
+    } else if (warp < WARP_GATHER0 + NUM_GATHER_WARPS) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_GATHER) : "memory");
+        gather_role<TWO>(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_OTHER) : "memory");
-        if (warp < WARP_GATHER0 + NUM_GATHER_WARPS)
-            gather_role(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
-        else if (warp == WARP_CONTROL)
-            control_role(p, smem, sbase, lane, abort_flag);
+        // the last warpgroup: control warp, MMA warp and two warps without a role
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LAST) : "memory");
+        if (warp == WARP_CONTROL)
+            control_role<TWO>(p, smem, sbase, lane, abort_flag);
         else if (warp == WARP_MMA && lane == 0)
             mma_role(p, smem, sbase, tmem, abort_flag);
     }
@@ -1085,7 +1115,10 @@ size_t attn_workspace_bytes(int64_t BT, int K, int num_sms)
 
 cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
 {
-    cudaError_t ea = cudaFuncSetAttribute(attn::attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the two-source build only when a second source is in use
+    const bool two = p.kv2 != nullptr && p.W < p.N;
+    void (*kernel)(AttnParams) = two ? attn::attn_kernel<true> : attn::attn_kernel<false>;
+    cudaError_t ea = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)attn::SMEM_BYTES);
     if (ea != cudaSuccess)
         return ea;
@@ -1107,7 +1140,7 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = s.split ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn::attn_kernel, p);
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace sa

@@ -18,7 +18,13 @@ constexpr size_t WS_HEADER = 256;
 
 struct AttnParams {
     CUtensorMap tm_q;          // q as 2-D [B*T*H rows, D cols] bf16, box 64x64, 128B swizzle
-    const uint16_t *kv;        // bf16 [B, N, D]: device memory or page-locked host memory
+    // latent rows, bf16 [.., D], device memory or page-locked host memory: list
+    // index v < W is row v of source 0, index v >= W is row v - W of source 1
+    // (one source: W = N); each source has its own batch stride, in rows
+    const uint16_t *kv;
+    const uint16_t *kv2;
+    int64_t kv_bstride, kv2_bstride;
+    int W;
     const int32_t *idx;        // int32 [B*T, K]
     const float *sink;         // fp32 [H]
     void *out;                 // [B*T, H, D] bf16 or fp32

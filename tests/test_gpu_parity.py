@@ -253,3 +253,39 @@ def test_kv_in_pinned_host_memory():
                               gd["idx"].data_ptr(), 0.1, 1, T, 64, 512, N, K, out.data_ptr(), 1,
                               ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
     assert code == 1   # SA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,T,K,W,C,host_c", [
+    (4, 1, 640, 128, 4096, False),    # decode shape, split schedule
+    (1, 40, 300, 128, 600, False),    # whole queries per CTA
+    (2, 3, 200, 0, 500, False),       # compressed rows only
+    (2, 3, 100, 128, 0, False),       # window rows only
+    (3, 2, 256, 128, 900, True),      # compressed cache in page-locked host memory
+])
+def test_two_source_matches_concatenation(B, T, K, W, C, host_c):
+    """The window ring and the compressed cache read in place (caches larger
+    than the rows in use, their padding NaN) give exactly the result of one
+    kv made by concatenating the rows in use, and match the oracle."""
+    g = torch.Generator().manual_seed(B * 100 + K)
+    D = 512
+    nan_bf16 = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    win = torch.full((B + 1, W + 8, D), nan_bf16.item(), dtype=torch.bfloat16)
+    cmp_ = torch.full((B + 1, C + 16, D), nan_bf16.item(), dtype=torch.bfloat16)
+    win[:B, :W] = I.rms_rows(torch.randn(B, W, D, generator=g)).to(torch.bfloat16)
+    cmp_[:B, :C] = I.rms_rows(torch.randn(B, C, D, generator=g)).to(torch.bfloat16)
+    q = torch.randn(B, T, 64, D, generator=g).to(torch.bfloat16)
+    sink = torch.randn(64, generator=g)
+    idx = torch.randint(0, W + C, (B, T, K), generator=g, dtype=torch.int32)
+    idx[torch.rand(B, T, K, generator=g) < 0.1] = -1
+    gd = to_dev(dict(q=q, sink=sink, idx=idx))
+    win_d = win.cuda() if W else None
+    cmp_d = (cmp_.pin_memory() if host_c else cmp_.cuda()) if C else None
+    got = sa.sparse_attn_two_source(gd["q"], win_d, cmp_d, gd["sink"], gd["idx"], 512 ** -0.5,
+                                    W=W, C=C, out_dtype=torch.float32, check=True)
+    cat = torch.cat([win[:B, :W], cmp_[:B, :C]], dim=1).contiguous()
+    one = sa.sparse_attn(gd["q"], cat.cuda(), gd["sink"], gd["idx"], 512 ** -0.5,
+                         out_dtype=torch.float32, check=True)
+    assert torch.equal(got, one)
+    ref, bad = oracle.sparse_attn_two_source(q, win, W, cmp_, C, sink, idx, 512 ** -0.5)
+    assert bad == 0
+    compare(got.double().cpu().numpy(), ref, f"two sources B{B} W{W} C{C}")

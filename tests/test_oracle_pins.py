@@ -296,3 +296,62 @@ def test_wo_a_block_diagonal_dense():
     y = oracle.wo_a(o, W)
     np.testing.assert_allclose(y.reshape(n, G * R), o.reshape(n, G * Din) @ full.T,
                                rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ two latent sources
+
+def _two_sources(B, Bmax, W, Wmax, C, Cmax, D, seed):
+    """Window and compressed caches larger than the rows in use, padding = NaN."""
+    rng = np.random.default_rng(seed)
+    nan = float("nan")
+    win = np.full((Bmax, Wmax, D), nan, dtype=np.float32)
+    cmp_ = np.full((Bmax, Cmax, D), nan, dtype=np.float32)
+    win[:B, :W] = rng.standard_normal((B, W, D))
+    cmp_[:B, :C] = rng.standard_normal((B, C, D))
+    return bf16(win), bf16(cmp_)
+
+
+def test_two_source_padding_is_never_read():
+    """Rows of either cache beyond W / C (and spare batch rows) hold NaN and
+    never reach the output; the result is sparse_attn on the rows in use."""
+    B, T, H, D, W, C, K = 2, 3, 4, 8, 5, 9, 10
+    win, cmp_ = _two_sources(B, 3, W, 7, C, 12, D, seed=3)
+    rng = np.random.default_rng(4)
+    q = bf16(rng.standard_normal((B, T, H, D)))
+    sink = rng.standard_normal(H).astype(np.float32)
+    idx = rng.integers(-1, W + C, size=(B, T, K)).astype(np.int32)
+    out, bad = oracle.sparse_attn_two_source(q, win, W, cmp_, C, sink, idx, 0.3)
+    assert bad == 0 and np.all(np.isfinite(out))
+    used = torch.cat([win[:B, :W], cmp_[:B, :C]], dim=1)
+    ref, _ = oracle.sparse_attn(q, used, sink, idx, 0.3)
+    assert np.array_equal(out, ref)
+
+
+@pytest.mark.parametrize("v", [0, 4, 5, 13])
+def test_two_source_index_reaches_the_right_row(v):
+    """q = 0 and sink = -inf make the output the mean of the listed rows: a
+    list holding only index v returns window row v (v < W) or compressed row
+    v - W (v >= W), exactly."""
+    B, T, H, D, W, C = 1, 1, 2, 8, 5, 9
+    win, cmp_ = _two_sources(B, 1, W, 6, C, 10, D, seed=5)
+    q = bf16(np.zeros((B, T, H, D)))
+    sink = np.full(H, -np.inf, dtype=np.float32)
+    idx = np.array([[[v, -1, -1]]], dtype=np.int32)
+    out, bad = oracle.sparse_attn_two_source(q, win, W, cmp_, C, sink, idx, 1.0)
+    row = win[0, v] if v < W else cmp_[0, v - W]
+    assert bad == 0
+    assert np.array_equal(out[0, 0, 0], f64(row)) and np.array_equal(out[0, 0, 1], f64(row))
+
+
+def test_two_source_one_source_empty():
+    """W = 0 reads only the compressed cache; C = 0 only the window."""
+    B, T, H, D = 1, 2, 2, 8
+    win, cmp_ = _two_sources(B, 1, 6, 6, 7, 7, D, seed=6)
+    rng = np.random.default_rng(7)
+    q = bf16(rng.standard_normal((B, T, H, D)))
+    sink = rng.standard_normal(H).astype(np.float32)
+    idx = rng.integers(0, 6, size=(B, T, 4)).astype(np.int32)
+    only_w, _ = oracle.sparse_attn_two_source(q, win, 6, None, 0, sink, idx, 0.5)
+    only_c, _ = oracle.sparse_attn_two_source(q, None, 0, cmp_, 7, sink, idx, 0.5)
+    assert np.array_equal(only_w, oracle.sparse_attn(q, win, sink, idx, 0.5)[0])
+    assert np.array_equal(only_c, oracle.sparse_attn(q, cmp_[:, :7], sink, idx, 0.5)[0])
