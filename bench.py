@@ -70,6 +70,9 @@ def algorithmic(wl: I.Workload, idx: torch.Tensor) -> dict:
         din = wl.H * wl.D // wl.G
         flops += 2 * wl.n_queries * wl.G * wl.R * din
         nbytes += wl.G * wl.R * din * 2 + wl.n_queries * wl.G * wl.R * 2 - wl.n_queries * wl.H * wl.D * 2
+    if wl.wo_b:
+        flops += 2 * wl.n_queries * wl.G * wl.R * wl.dim
+        nbytes += wl.dim * wl.G * wl.R * 2 + wl.n_queries * (wl.dim - wl.G * wl.R) * 2
     return {"pairs": pairs, "bytes": nbytes, "flops": flops}
 
 
@@ -247,10 +250,11 @@ def time_graph_steps(step_fns, steps: int, warmup: int):
 # ------------------------------------------------------------------ our arm
 
 def launches_per_call(wl: I.Workload, num_sms: int) -> int:
-    """Kernels one call enqueues: the attention kernel, plus the piece combine
-    when there are fewer queries than SMs, plus the grouped GEMM of the tail."""
-    n = 1 + (1 if wl.n_queries < num_sms and wl.K > 0 else 0)
-    return n + (1 if wl.tail else 0)
+    """Kernels one call enqueues: the attention kernel (the list pieces of a
+    query merge inside their cluster, with no second kernel), plus the grouped
+    GEMM of the tail, plus the wo_b GEMM of the block tail."""
+    del num_sms
+    return 1 + (1 if wl.tail else 0) + (1 if wl.wo_b else 0)
 
 
 def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_sets=None):
@@ -259,7 +263,17 @@ def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_se
     sets = sets_for(wl, dev, n_sets=n_sets)
     outs = []
     fns = []
-    if wl.tail:
+    if wl.wo_b:
+        rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).to(dev)
+        for x in sets:
+            z = torch.empty((wl.B, wl.T, wl.dim), dtype=torch.bfloat16, device=dev)
+            ws = torch.zeros(sa.block_tail_workspace_size(wl.B, wl.T, wl.K, wl.G, wl.R),
+                             dtype=torch.uint8, device=dev)
+            outs.append((z, ws))
+            fns.append(lambda x=x, z=z, ws=ws: sa.sparse_attn_block_tail(
+                x["q"], x["kv"], x["sink"], x["idx"], wl.scale, rope, x["wo_a"], x["wo_b"], out=z,
+                workspace=ws))
+    elif wl.tail:
         rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).to(dev)
         for x in sets:
             y = torch.empty((wl.B, wl.T, wl.G * wl.R), dtype=torch.bfloat16, device=dev)
@@ -418,11 +432,11 @@ def run_ours(args):
         return
     extra = {}
     if not args.headline_only and world == 1:
-        for name in ("long_decode", "prefill", "fused_tail"):
+        for name in ("long_decode", "prefill", "fused_tail", "block_tail"):
             steps = max(3, min(args.steps, 20))
             r = bench_workload(name, steps, max(args.warmup, 3), dev, with_e2e=False)
             r["clocks"] = sampler.summary(*r.pop("window"))
-            if name in ("prefill", "fused_tail"):
+            if name in ("prefill", "fused_tail", "block_tail"):
                 r["roofline"] = {"bound": "tensor", "achieved": r["tflops"],
                                  "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
                                  "frac": r["tflops"] / pk["bf16_tflops_sustained"],

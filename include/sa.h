@@ -136,7 +136,7 @@ size_t sa_sparse_attn_rope_wo_a_workspace_size(int B, int T, int H, int D, int K
  *          pos_t * w_i for the frequency pairs i of query t (same for every
  *          batch row; see sa_rope_table).  Feature pair i is (D - rope_dim + 2i,
  *          D - rope_dim + 2i + 1), rotated as one complex number by -pos_t*w_i.
- *   rope_dim 64 (even, <= D)
+ *   rope_dim 64 (a multiple of 32, <= D)
  *   wo_a   bf16 [G, R, H*D/G] contiguous, 16-byte aligned ([out, in] per group)
  *   G, R   8 groups x 1024 rank on the fast path
  *   out    bf16 [B, T, G*R] contiguous, 16-byte aligned
@@ -147,6 +147,33 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
                                    const float *rope_cos_sin, int rope_dim,
                                    const void *wo_a, int G, int R, void *out,
                                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Bytes of workspace `sa_sparse_attn_block_tail` needs: the fused call's
+ * workspace plus the bf16 wo_a output [B, T, G*R] kept between the GEMMs.
+ */
+size_t sa_sparse_attn_block_tail_workspace_size(int B, int T, int H, int D, int K,
+                                                int G, int R);
+
+/*
+ * The whole tail of the same page's Attention.forward: sa_sparse_attn_rope_wo_a,
+ * then `x = self.wo_b(o.flatten(2))` -- the "Output projection" page's wo_b,
+ * a linear map of the G*R = 8192 group features to the model width (5120)
+ * without bias, weight stored [out, in] like every module of the page.  On one
+ * GPU its row-parallel all-reduce is the identity.
+ *   (q ... R) as for sa_sparse_attn_rope_wo_a
+ *   wo_b   bf16 [dim, G*R] contiguous, 16-byte aligned
+ *   dim    model width, a multiple of 256 (5120)
+ *   out    bf16 [B, T, dim] contiguous, 16-byte aligned
+ * The wo_a output is rounded to bf16 between the two products, as the page's
+ * bf16 einsum does.
+ */
+sa_status sa_sparse_attn_block_tail(const void *q, const void *kv, const float *sink,
+                                    const int32_t *idx, float scale, int B, int T, int H,
+                                    int D, int N, int K, const float *rope_cos_sin,
+                                    int rope_dim, const void *wo_a, int G, int R,
+                                    const void *wo_b, int dim, void *out, void *workspace,
+                                    size_t ws_bytes, void *stream);
 
 /*
  * Host helper: fill cos_sin_host fp32 [T, rope_dim/2, 2] with

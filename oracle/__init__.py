@@ -161,6 +161,18 @@ def inverse_rope(o: np.ndarray, pos, rope_dim: int, theta: float, n_threads: int
     return x
 
 
+def wo_b(y: np.ndarray, W) -> np.ndarray:
+    """``x = self.wo_b(o.flatten(2))`` of the "DeepSeek-V4.1 > Output projection"
+    page: a bias-free linear map, weight bf16 [dim, G*R] ([out, in]);
+    y fp64 [n, G*R] -> fp64 [n, dim] (one fp64 matrix product)."""
+    w = _as_bf16_bits(W).astype(np.uint32) << 16
+    w = w.view(np.float32).astype(np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    if y.ndim != 2 or w.ndim != 2 or y.shape[1] != w.shape[1]:
+        raise ValueError("shape mismatch")
+    return y @ w.T
+
+
 def wo_a(o: np.ndarray, W, n_threads: int = 0):
     """Grouped projection: o fp64 [n, G, Din], W bf16 [G, R, Din] -> fp64 [n, G, R]."""
     x = np.ascontiguousarray(o, dtype=np.float64)

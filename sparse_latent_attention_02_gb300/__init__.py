@@ -18,7 +18,7 @@ import torch
 
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
-__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_rope_wo_a", "rope_table", "workspace_size",
+__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_rope_wo_a", "sparse_attn_block_tail", "rope_table", "workspace_size",
            "fused_workspace_size", "check_errors", "SAError", "library", "build"]
 
 HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
@@ -26,7 +26,8 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_
            4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA"}
 EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_two_source",
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
-           "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc")
+           "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
+           "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail")
 
 
 class SAError(RuntimeError):
@@ -64,6 +65,11 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_sparse_attn_rope_wo_a.restype = I
             lib.sa_sparse_attn_rope_wo_a.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
                                                      V, V, Z, V]
+            lib.sa_sparse_attn_block_tail_workspace_size.restype = Z
+            lib.sa_sparse_attn_block_tail_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            lib.sa_sparse_attn_block_tail.restype = I
+            lib.sa_sparse_attn_block_tail.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
+                                                      V, I, V, V, Z, V]
             lib.sa_rope_table.restype = I
             lib.sa_rope_table.argtypes = [D, I, I, I, V]
             lib.sa_check_errors.restype = I
@@ -275,6 +281,53 @@ def sparse_attn_rope_wo_a(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor,
     if check:
         check_errors(workspace, stream)
     return out
+
+
+def sparse_attn_block_tail(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor,
+                           idx: torch.Tensor, scale: float, rope_cos_sin: torch.Tensor,
+                           wo_a: torch.Tensor, wo_b: torch.Tensor, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None, stream=None,
+                           check: bool = False) -> torch.Tensor:
+    """The attention block's tail: sparse_attn, inverse RoPE, grouped wo_a, then wo_b.
+
+    rope_cos_sin fp32 [T, rope_dim/2, 2]; wo_a bf16 [G, R, H*D/G]; wo_b bf16 [dim, G*R]
+    ([out, in]); returns bf16 [B, T, dim].
+    """
+    B, T, H, D, N, K = _attn_args(q, kv, sink, idx)
+    _need(rope_cos_sin, "rope_cos_sin", torch.float32, 3)
+    _need(wo_a, "wo_a", torch.bfloat16, 3)
+    _need(wo_b, "wo_b", torch.bfloat16, 2)
+    G, R, Din = wo_a.shape
+    dim = wo_b.shape[0]
+    if rope_cos_sin.shape[0] != T or rope_cos_sin.shape[2] != 2:
+        raise ValueError("rope_cos_sin must be [T, rope_dim/2, 2]")
+    if G * Din != H * D:
+        raise ValueError("wo_a must be [G, R, H*D/G]")
+    if wo_b.shape[1] != G * R:
+        raise ValueError("wo_b must be [dim, G*R]")
+    rope_dim = 2 * rope_cos_sin.shape[1]
+    if out is None:
+        out = torch.empty((B, T, dim), dtype=torch.bfloat16, device=q.device)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+    lib = library()
+    need = int(lib.sa_sparse_attn_block_tail_workspace_size(B, T, H, D, K, G, R))
+    if workspace is None:
+        workspace = _workspace(need, q.device, "tail")
+    code = lib.sa_sparse_attn_block_tail(q.data_ptr(), kv.data_ptr(), sink.data_ptr(), idx.data_ptr(),
+                                         float(scale), B, T, H, D, N, K, rope_cos_sin.data_ptr(),
+                                         rope_dim, wo_a.data_ptr(), G, R, wo_b.data_ptr(), dim,
+                                         out.data_ptr(), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream_ptr(stream))
+    _check(code, "sa_sparse_attn_block_tail")
+    if check:
+        check_errors(workspace, stream)
+    return out
+
+
+def block_tail_workspace_size(B: int, T: int, K: int, G: int, R: int) -> int:
+    return int(library().sa_sparse_attn_block_tail_workspace_size(B, T, HEADS, HEAD_DIM, K, G, R))
 
 
 def rope_table(theta: float, start_pos: int, T: int, rope_dim: int = 64) -> torch.Tensor:

@@ -130,6 +130,26 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const KvSources &src, c
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// y[m, g*R + r] = sum_d a[m, g*Din + d] * w[g*R + r, d] for m < M (bf16 in and
+// out, fp32 accumulation) on the persistent tcgen05 GEMM.
+sa_status grouped_gemm(const void *a, const void *w, void *y, int64_t M, int G, int R, int Din, void *ws,
+                       int sms, cudaStream_t s)
+{
+    GemmParams g;
+    std::memset(&g, 0, sizeof g);
+    if (!encode_tmap_2d(&g.tm_a, a, (uint64_t)M, (uint64_t)G * Din, 64, 128) ||
+        !encode_tmap_2d(&g.tm_b, w, (uint64_t)G * R, (uint64_t)Din, 64, 256))
+        return SA_ERR_CUDA;
+    g.y = static_cast<uint16_t *>(y);
+    g.err = static_cast<uint32_t *>(ws);
+    g.M = (int)M;
+    g.G = G;
+    g.R = R;
+    g.Din = Din;
+    g.timeout_ns = wait_timeout_ns();
+    return launch_wo_a(g, sms, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
 }  // namespace
 
 // Checks shared by the attention entry points; nothing is enqueued before them.
@@ -286,6 +306,55 @@ size_t sa_sparse_attn_rope_wo_a_workspace_size(int B, int T, int H, int D, int K
     return round256(attn) + round256((size_t)B * T * H * D * 2);
 }
 
+namespace {
+
+// Host checks of the tail arguments.  rope_dim is a multiple of 32 so that
+// every warp of the epilogue either rotates all of its 32 features or none.
+sa_status check_tail_args(int H, int D, const float *rope_cos_sin, int rope_dim, const void *wo_a, int G,
+                          int R)
+{
+    if (G <= 0 || R <= 0 || rope_dim < 0)
+        return SA_ERR_INVALID_ARG;
+    if ((H * D) % G != 0 || ((H * D) / G) % 64 != 0 || R % 256 != 0 || rope_dim % 32 != 0 || rope_dim > D)
+        return SA_ERR_UNSUPPORTED;
+    if (!wo_a || !aligned(wo_a, 16) || (rope_dim > 0 && !rope_cos_sin))
+        return SA_ERR_INVALID_ARG;
+    return SA_OK;
+}
+
+// Attention with the inverse RoPE in its epilogue (bf16 o kept in the
+// workspace after the attention's own part), then the grouped wo_a into y
+// [B*T, G*R] bf16.  Arguments already checked.
+sa_status attn_rope_wo_a(const void *q, const void *kv, const float *sink, const int32_t *idx, float scale,
+                         int B, int T, int H, int D, int N, int K, const float *rope_cos_sin, int rope_dim,
+                         const void *wo_a, int G, int R, void *y, void *workspace, size_t attn_ws, int sms,
+                         cudaStream_t s)
+{
+    const int64_t BT = (int64_t)B * T;
+    void *o = static_cast<uint8_t *>(workspace) + attn_ws;
+    // 1) sparse attention with the inverse rotary embedding fused into its
+    //    epilogue, bf16 output kept in the workspace
+    if (K == 0) {
+        if (cudaMemsetAsync(o, 0, (size_t)BT * H * D * 2, s) != cudaSuccess)
+            return SA_ERR_CUDA;
+    } else {
+        AttnParams p;
+        const KvSources src{kv, N, N, nullptr, 0};
+        const sa_status st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, o, false, workspace);
+        if (st != SA_OK)
+            return st;
+        p.rope = rope_cos_sin;
+        p.rope_dim = rope_dim;
+        const Schedule sch = attn_schedule(BT, K, sms);
+        if (launch_attention(p, sch, s) != cudaSuccess)
+            return SA_ERR_CUDA;
+    }
+    // 2) grouped wo_a
+    return grouped_gemm(o, wo_a, y, BT, G, R, H * D / G, workspace, sms, s);
+}
+
+}  // namespace
+
 sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *sink,
                                    const int32_t *idx, float scale, int B, int T, int H, int D,
                                    int N, int K, const float *rope_cos_sin, int rope_dim,
@@ -295,16 +364,12 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
     sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
     if (st != SA_OK)
         return st;
-    if (G <= 0 || R <= 0 || rope_dim < 0)
-        return SA_ERR_INVALID_ARG;
-    if ((H * D) % G != 0 || ((H * D) / G) % 64 != 0 || R % 256 != 0 || rope_dim % 4 != 0 ||
-        rope_dim > D)
-        return SA_ERR_UNSUPPORTED;
     const int64_t BT = (int64_t)B * T;
     if (BT == 0)
-        return SA_OK;
-    if (!wo_a || !aligned(wo_a, 16) || (rope_dim > 0 && !rope_cos_sin))
-        return SA_ERR_INVALID_ARG;
+        return G <= 0 || R <= 0 || rope_dim < 0 ? SA_ERR_INVALID_ARG : SA_OK;
+    st = check_tail_args(H, D, rope_cos_sin, rope_dim, wo_a, G, R);
+    if (st != SA_OK)
+        return st;
     if (BT >= ((int64_t)1 << 31) / 128)
         return SA_ERR_UNSUPPORTED;
     int sms = 0;
@@ -314,42 +379,57 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
     const size_t o_bytes = round256((size_t)BT * H * D * 2);
     if (ws_bytes < attn_ws + o_bytes)
         return SA_ERR_WORKSPACE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void *o = static_cast<uint8_t *>(workspace) + attn_ws;
+    return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, G, R, out,
+                          workspace, attn_ws, sms, static_cast<cudaStream_t>(stream));
+}
 
-    // 1) sparse attention with the inverse rotary embedding fused into its
-    //    epilogue, bf16 output kept in the workspace
-    if (K == 0) {
-        if (cudaMemsetAsync(o, 0, (size_t)BT * H * D * 2, s) != cudaSuccess)
-            return SA_ERR_CUDA;
-    } else {
-        AttnParams p;
-        const KvSources src{kv, N, N, nullptr, 0};
-        st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, o, false, workspace);
-        if (st != SA_OK)
-            return st;
-        p.rope = rope_cos_sin;
-        p.rope_dim = rope_dim;
-        const Schedule sch = attn_schedule(BT, K, sms);
-        if (launch_attention(p, sch, s) != cudaSuccess)
-            return SA_ERR_CUDA;
-    }
+size_t sa_sparse_attn_block_tail_workspace_size(int B, int T, int H, int D, int K, int G, int R)
+{
+    const size_t fused = sa_sparse_attn_rope_wo_a_workspace_size(B, T, H, D, K, G, R);
+    if (B < 0 || T < 0 || G < 0 || R < 0)
+        return fused;
+    return round256(fused) + round256((size_t)B * T * G * R * 2);
+}
 
-    // 2) grouped wo_a
-    GemmParams g;
-    std::memset(&g, 0, sizeof g);
-    const int Din = H * D / G;
-    if (!encode_tmap_2d(&g.tm_a, o, (uint64_t)BT, (uint64_t)H * D, 64, 128) ||
-        !encode_tmap_2d(&g.tm_b, wo_a, (uint64_t)G * R, (uint64_t)Din, 64, 256))
+sa_status sa_sparse_attn_block_tail(const void *q, const void *kv, const float *sink, const int32_t *idx,
+                                    float scale, int B, int T, int H, int D, int N, int K,
+                                    const float *rope_cos_sin, int rope_dim, const void *wo_a, int G, int R,
+                                    const void *wo_b, int dim, void *out, void *workspace, size_t ws_bytes,
+                                    void *stream)
+{
+    sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
+    if (st != SA_OK)
+        return st;
+    const int64_t BT = (int64_t)B * T;
+    if (BT == 0)
+        return G <= 0 || R <= 0 || rope_dim < 0 || dim <= 0 ? SA_ERR_INVALID_ARG : SA_OK;
+    st = check_tail_args(H, D, rope_cos_sin, rope_dim, wo_a, G, R);
+    if (st != SA_OK)
+        return st;
+    if (dim <= 0)
+        return SA_ERR_INVALID_ARG;
+    if (dim % 256 != 0 || ((int64_t)G * R) % 64 != 0)
+        return SA_ERR_UNSUPPORTED;
+    if (!wo_b || !aligned(wo_b, 16))
+        return SA_ERR_INVALID_ARG;
+    if (BT >= ((int64_t)1 << 31) / 128)
+        return SA_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (!current_sms(&sms))
         return SA_ERR_CUDA;
-    g.y = static_cast<uint16_t *>(out);
-    g.err = static_cast<uint32_t *>(workspace);
-    g.M = (int)BT;
-    g.G = G;
-    g.R = R;
-    g.Din = Din;
-    g.timeout_ns = wait_timeout_ns();
-    return launch_wo_a(g, sms, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+    const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
+    const size_t o_bytes = round256((size_t)BT * H * D * 2);
+    const size_t y_bytes = round256((size_t)BT * G * R * 2);
+    if (ws_bytes < attn_ws + o_bytes + y_bytes)
+        return SA_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *y = static_cast<uint8_t *>(workspace) + attn_ws + o_bytes;
+    st = attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, G, R, y,
+                        workspace, attn_ws, sms, s);
+    if (st != SA_OK)
+        return st;
+    // 3) wo_b: one dense [dim, G*R] projection of the flattened groups
+    return grouped_gemm(y, wo_b, out, BT, 1, dim, G * R, workspace, sms, s);
 }
 
 sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim, float *cos_sin_host)

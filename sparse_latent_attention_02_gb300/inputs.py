@@ -46,6 +46,9 @@ class Workload:
     R: int = 1024       # o_lora_rank
     rope_dim: int = 64  # rope_head_dim
     theta: float = 160000.0   # compress_rope_theta
+    # block tail: the fused tail, then wo_b (G*R group features -> dim)
+    wo_b: bool = False
+    dim: int = 5120
 
     @property
     def N(self) -> int:
@@ -77,6 +80,9 @@ WORKLOADS = {
     # two 4096-token prefills, then inverse RoPE and grouped wo_a
     "fused_tail": Workload("fused_tail", B=2, T=4096, H=64, D=512, W=128, C=4096,
                            ratio=2, K=640, pos0=0, topk=512, kind="prefill", tail=True),
+    # the same, continued through wo_b to the model width
+    "block_tail": Workload("block_tail", B=2, T=4096, H=64, D=512, W=128, C=4096,
+                           ratio=2, K=640, pos0=0, topk=512, kind="prefill", tail=True, wo_b=True),
 }
 
 
@@ -182,7 +188,8 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
 
     q ~ N(0,1) bf16 [B,T,H,D]; kv rows N(0,1), RMS-normalised in fp32, bf16
     [B,N,D]; sink ~ N(0,1) fp32 [H]; idx int32 [B,T,K]; pos int64 [B,T].  With
-    the fused tail also W ~ N(0, 0.02) bf16 [G, R, H*D/G] drawn from seed+1.
+    the fused tail also W ~ N(0, 0.02) bf16 [G, R, H*D/G] drawn from seed+1, and
+    with the block tail wo_b ~ N(0, 0.02) bf16 [dim, G*R] drawn from seed+2.
     """
     device = torch.device(device)
     g = _gen(seed, device)
@@ -200,5 +207,9 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
         gw = _gen(seed + 1, device)
         din = wl.H * wl.D // wl.G
         out["wo_a"] = (0.02 * torch.randn((wl.G, wl.R, din), generator=gw, device=device,
+                                          dtype=torch.float32)).to(torch.bfloat16)
+    if wl.wo_b:
+        gb = _gen(seed + 2, device)
+        out["wo_b"] = (0.02 * torch.randn((wl.dim, wl.G * wl.R), generator=gb, device=device,
                                           dtype=torch.float32)).to(torch.bfloat16)
     return out

@@ -92,6 +92,28 @@ def test_fused_argument_checks(lib):
     assert call(H=16) == UNSUPPORTED
 
 
+def test_block_tail_argument_checks(lib):
+    def call(**kw):
+        a = dict(q=16, kv=16, sink=16, idx=16, scale=0.1, B=1, T=1, H=64, D=512, N=8, K=4,
+                 rope=16, rope_dim=64, wa=16, G=8, R=1024, wb=16, dim=5120, out=16, ws=256,
+                 wsb=1 << 31, stream=None)
+        a.update(kw)
+        return lib.sa_sparse_attn_block_tail(a["q"], a["kv"], a["sink"], a["idx"], a["scale"],
+                                             a["B"], a["T"], a["H"], a["D"], a["N"], a["K"],
+                                             a["rope"], a["rope_dim"], a["wa"], a["G"], a["R"],
+                                             a["wb"], a["dim"], a["out"], a["ws"], a["wsb"],
+                                             a["stream"])
+    assert call(dim=0) == INVALID
+    assert call(dim=5000) == UNSUPPORTED          # not a multiple of 256
+    assert call(wb=None) == INVALID
+    assert call(wb=8) == INVALID                  # 16-byte alignment
+    assert call(rope_dim=16) == UNSUPPORTED       # rotated features must fill whole warps (32)
+    assert call(G=3) == UNSUPPORTED
+    n = lib.sa_sparse_attn_block_tail_workspace_size(2, 4096, 64, 512, 640, 8, 1024)
+    f = lib.sa_sparse_attn_rope_wo_a_workspace_size(2, 4096, 64, 512, 640, 8, 1024)
+    assert n >= f + 2 * 4096 * 8 * 1024 * 2 and n % 256 == 0
+
+
 def test_workspace_size_queries(lib):
     # without a device the size falls back to one SM; it is always >= 256, 256-aligned
     for B, T, K in [(1, 16, 192), (64, 1, 640), (1, 8192, 640), (0, 0, 0)]:

@@ -289,3 +289,22 @@ def test_two_source_matches_concatenation(B, T, K, W, C, host_c):
     ref, bad = oracle.sparse_attn_two_source(q, win, W, cmp_, C, sink, idx, 512 ** -0.5)
     assert bad == 0
     compare(got.double().cpu().numpy(), ref, f"two sources B{B} W{W} C{C}")
+
+
+def test_block_tail_workload_sampled():
+    """sparse_attn -> inverse RoPE -> grouped wo_a -> wo_b on the block-tail
+    workload, sampled rows against the fp64 chain of oracle steps."""
+    wl = I.WORKLOADS["block_tail"]
+    x = I.make_inputs(wl, seed=4, device="cuda")
+    rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).cuda()
+    z = sa.sparse_attn_block_tail(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, rope, x["wo_a"],
+                                  x["wo_b"], check=True)
+    qs = sample_queries(wl.n_queries, 16, seed=5, include=(0, 4095, 4096, 8191))
+    o = oracle_rows(x, qs, wl.scale)
+    o = oracle.inverse_rope(o, qs % wl.T, wl.rope_dim, wl.theta)
+    y = oracle.wo_a(o.reshape(len(qs), wl.G, -1), x["wo_a"].cpu())
+    zref = oracle.wo_b(y.reshape(len(qs), -1), x["wo_b"].cpu())
+    got = z.reshape(-1, wl.dim)[torch.as_tensor(qs, device="cuda")].double().cpu().numpy()
+    # wo_b's outputs reach several units: each may also differ by 2^-7 of its magnitude
+    # (its own bf16 rounding is 2^-9)
+    compare(got, zref, "block_tail", per_value=True)

@@ -355,3 +355,21 @@ def test_two_source_one_source_empty():
     only_c, _ = oracle.sparse_attn_two_source(q, None, 0, cmp_, 7, sink, idx, 0.5)
     assert np.array_equal(only_w, oracle.sparse_attn(q, win, sink, idx, 0.5)[0])
     assert np.array_equal(only_c, oracle.sparse_attn(q, cmp_[:, :7], sink, idx, 0.5)[0])
+
+
+# ------------------------------------------------------------------ wo_b
+
+def test_wo_b_equals_one_group_wo_a_and_a_hand_case():
+    """wo_b (one fp64 matrix product) against the independent grouped loop of
+    wo_a with a single group, and a 2 x 2 case worked by hand."""
+    rng = np.random.default_rng(11)
+    n, din, dim = 5, 64, 48
+    y = rng.standard_normal((n, din))
+    W = bf16(0.1 * rng.standard_normal((dim, din)))
+    got = oracle.wo_b(y, W)
+    ref = oracle.wo_a(y.reshape(n, 1, din), W.reshape(1, dim, din)).reshape(n, dim)
+    assert np.allclose(got, ref, rtol=1e-13, atol=1e-13)
+    # [[1, 2], [3, 4]] @ [[1, 0.5], [-2, 0.25]]^T = [[2, -1.5], [5, -5]]
+    yh = np.array([[1.0, 2.0], [3.0, 4.0]])
+    Wh = bf16([[1.0, 0.5], [-2.0, 0.25]])
+    assert np.array_equal(oracle.wo_b(yh, Wh), np.array([[2.0, -1.5], [5.0, -5.0]]))
