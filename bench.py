@@ -386,6 +386,32 @@ def bench_e2e(wl: I.Workload, x: dict, steps: int, warmup: int, dev) -> dict:
                     f"output copied back; copies, calls and read-backs pipelined on three streams"}
 
 
+def bench_topk(steps: int, warmup: int, dev, pk: dict) -> dict:
+    """Top-k selection of 512 of 4096 compressed positions for the 8192 queries
+    of the prefill workload (scores N(0,1), each query's visible prefix
+    causal): one call per step, inputs rotating over sets larger than L2."""
+    import sparse_latent_attention_02_gb300 as sa
+    rows, L, k = 8192, 4096, 512
+    n_sets = 3
+    sets = []
+    vis = (torch.arange(rows, device=dev) // 2 + 1).clamp(max=L)
+    cols = torch.arange(L, device=dev)
+    for i in range(n_sets):
+        g = torch.Generator(device=dev).manual_seed(100 + i)
+        sc = torch.randn((rows, L), generator=g, device=dev)
+        sc[cols[None, :] >= vis[:, None]] = float("-inf")
+        sets.append((sc, torch.empty((rows, k), dtype=torch.int32, device=dev)))
+    fns = [lambda sc=sc, o=o: sa.topk_indices(sc, k, offset=128, out=o) for sc, o in sets]
+    secs, _ = time_graph_steps(fns, steps, warmup)
+    step_s = secs / steps
+    nbytes = rows * L * 4 + rows * k * 4
+    gbs = nbytes / step_s / 1e9
+    return {"workload": f"topk: {rows} rows x {L} positions -> {k}", "ms_per_step": step_s * 1e3,
+            "rows_per_s": rows / step_s, "gbs": gbs, "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "peak_note": f"{pk['source']} HBM copy"}}
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
     """The fp64 oracle, as it stands, on the host cores: whole decode steps
     (all queries of one input set) repeated until about `budget_s` seconds."""
@@ -448,6 +474,7 @@ def run_ours(args):
                                  "traffic": measured_traffic(name),
                                  "peak_note": f"{pk['source']} HBM copy"}
             extra[name] = r
+        extra["topk"] = bench_topk(max(3, min(args.steps, 50)), max(args.warmup, 3), dev, pk)
     sampler.stop()
     e2e = head.pop("e2e", None)
     cpu = (cpu_baseline(args.workload, budget_s=args.cpu_seconds)

@@ -176,6 +176,23 @@ sa_status sa_sparse_attn_block_tail(const void *q, const void *kv, const float *
                                     size_t ws_bytes, void *stream);
 
 /*
+ * Top-k selection of compressed positions, the step that produces the
+ * compressed part of the index lists (the "DeepSeek-V4.1 > 40 layers" page's
+ * `_compress_topk_idxs`: the indexer returns int32 positions, `index_topk` =
+ * 512 of them, offset by the window length `kv.size(1)`).  The indexer's
+ * scoring is not on the pages; this is the selection over given scores:
+ *   scores fp32, row r at scores + r * row_stride, L positions per row;
+ *          a score of -inf or NaN marks a position that may not be chosen
+ *   out    int32 [rows, k]: the positions of the k largest scores (ties to
+ *          the smaller position), in ascending order, each plus `offset`;
+ *          -1 after them when a row has fewer than k positions to choose
+ * Device memory; asynchronous on `stream`.  SA_ERR_INVALID_ARG for negative
+ * sizes, row_stride < L, offset < 0 or null / misaligned (4-byte) pointers.
+ */
+sa_status sa_topk_indices(const float *scores, int64_t row_stride, int64_t rows, int L,
+                          int k, int offset, int32_t *out, void *stream);
+
+/*
  * Host helper: fill cos_sin_host fp32 [T, rope_dim/2, 2] with
  * (cos, sin)((start_pos + t) * theta ** (-2i / rope_dim)), computed in double.
  * This is the precomputed rotary table of Attention.__init__ (plain theta, no

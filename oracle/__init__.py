@@ -146,6 +146,26 @@ def sparse_attn_two_source(q, window_kv, W: int, compressed_kv, C: int, sink, id
     return sparse_attn(qb, np.ascontiguousarray(kv), sink, idx, scale, queries=queries, n_threads=n_threads)
 
 
+def topk_indices(scores, k: int, offset: int = 0) -> np.ndarray:
+    """Top-k selection of compressed positions (the "DeepSeek-V4.1 > 40 layers"
+    page's `_compress_topk_idxs`: int32 positions offset by the window length,
+    -1 where fewer exist), over given scores: per row the positions of the k
+    largest scores that are not -inf or NaN, ties to the smaller position,
+    returned in ascending order plus ``offset``, then -1.
+    scores float [..., L] -> int32 [..., k] (one stable sort per row)."""
+    a = np.asarray(scores, dtype=np.float64)
+    L = a.shape[-1]
+    rows = a.reshape(int(np.prod(a.shape[:-1], dtype=np.int64)), L)
+    out = np.full((rows.shape[0], k), -1, dtype=np.int64)
+    for r, row in enumerate(rows):
+        pos = np.nonzero(~(np.isnan(row) | (row == -np.inf)))[0]
+        # descending score, then ascending position
+        order = pos[np.lexsort((pos, -row[pos]))][:k]
+        chosen = np.sort(order)
+        out[r, :chosen.size] = chosen + offset
+    return out.reshape(*a.shape[:-1], k).astype(np.int32)
+
+
 def inverse_rope(o: np.ndarray, pos, rope_dim: int, theta: float, n_threads: int = 0):
     """In-place-free inverse rotary embedding of the last ``rope_dim`` features.
 

@@ -18,7 +18,8 @@ import torch
 
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
-__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_rope_wo_a", "sparse_attn_block_tail", "rope_table", "workspace_size",
+__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_rope_wo_a", "sparse_attn_block_tail",
+           "topk_indices", "rope_table", "workspace_size",
            "fused_workspace_size", "check_errors", "SAError", "library", "build"]
 
 HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
@@ -27,7 +28,8 @@ _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_
 EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_two_source",
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
-           "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail")
+           "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail",
+           "sa_topk_indices")
 
 
 class SAError(RuntimeError):
@@ -70,6 +72,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_sparse_attn_block_tail.restype = I
             lib.sa_sparse_attn_block_tail.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
                                                       V, I, V, V, Z, V]
+            lib.sa_topk_indices.restype = I
+            lib.sa_topk_indices.argtypes = [V, ctypes.c_int64, ctypes.c_int64, I, I, I, V, V]
             lib.sa_rope_table.restype = I
             lib.sa_rope_table.argtypes = [D, I, I, I, V]
             lib.sa_check_errors.restype = I
@@ -323,6 +327,36 @@ def sparse_attn_block_tail(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor
     _check(code, "sa_sparse_attn_block_tail")
     if check:
         check_errors(workspace, stream)
+    return out
+
+
+def topk_indices(scores: torch.Tensor, k: int, offset: int = 0, out: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """Positions of the k largest scores per row (-inf / NaN never chosen, ties
+    to the smaller position), ascending, plus ``offset``; -1 padded.
+
+    scores fp32 [..., L] on the GPU (rows of unit stride); returns int32 [..., k].
+    """
+    if not isinstance(scores, torch.Tensor) or scores.dtype != torch.float32 or scores.dim() < 1:
+        raise TypeError("scores must be an fp32 tensor [..., L]")
+    if not scores.is_cuda:
+        raise ValueError("scores must live on a CUDA device")
+    if scores.stride(-1) != 1:
+        raise ValueError("scores rows must be contiguous")
+    L = scores.shape[-1]
+    lead = scores.shape[:-1]
+    rows = 1
+    for n in lead:
+        rows *= int(n)
+    flat = scores.reshape(rows, L)
+    if out is None:
+        out = torch.empty((*lead, k), dtype=torch.int32, device=scores.device)
+    elif out.dtype != torch.int32 or out.shape != (*lead, k) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int32 [..., k]")
+    code = library().sa_topk_indices(flat.data_ptr() if L > 0 else None,
+                                     flat.stride(0) if rows > 0 else L, rows, L, int(k), int(offset),
+                                     out.data_ptr() if out.numel() else None, _stream_ptr(stream))
+    _check(code, "sa_topk_indices")
     return out
 
 

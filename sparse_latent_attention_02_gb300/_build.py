@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsa.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["sa_attn.cu", "sa_gemm.cu", "sa_api.cu", "sa_noalloc.cu"]
+SOURCES = ["sa_attn.cu", "sa_gemm.cu", "sa_topk.cu", "sa_api.cu", "sa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

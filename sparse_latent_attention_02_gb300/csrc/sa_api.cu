@@ -432,6 +432,23 @@ sa_status sa_sparse_attn_block_tail(const void *q, const void *kv, const float *
     return grouped_gemm(y, wo_b, out, BT, 1, dim, G * R, workspace, sms, s);
 }
 
+sa_status sa_topk_indices(const float *scores, int64_t row_stride, int64_t rows, int L, int k, int offset,
+                          int32_t *out, void *stream)
+{
+    if (rows < 0 || L < 0 || k < 0 || row_stride < L || rows >= ((int64_t)1 << 31))
+        return SA_ERR_INVALID_ARG;
+    if ((int64_t)L + offset >= ((int64_t)1 << 31) || offset < 0)
+        return SA_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0)
+        return SA_OK;
+    if (!out || !aligned(out, 4) || (L > 0 && (!scores || !aligned(scores, 4))))
+        return SA_ERR_INVALID_ARG;
+    return launch_topk(scores, row_stride, rows, L, k, offset, out, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SA_OK
+               : SA_ERR_CUDA;
+}
+
 sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim, float *cos_sin_host)
 {
     if (T < 0 || rope_dim <= 0 || rope_dim % 2 != 0 || !(theta > 0.0) || start_pos < 0)

@@ -69,6 +69,10 @@ struct GemmParams {
 
 cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st);
 
+// Top-k selection of positions per row of scores (see sa_topk_indices).
+cudaError_t launch_topk(const float *scores, int64_t row_stride, int64_t rows, int L, int k, int offset,
+                        int32_t *out, cudaStream_t st);
+
 // Host argument checks of the attention entry points (no CUDA call).
 sa_status check_attn_args(const void *q, const void *kv, const float *sink, const int32_t *idx,
                           float scale, int B, int T, int H, int D, int N, int K, const void *out,

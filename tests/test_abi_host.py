@@ -114,6 +114,19 @@ def test_block_tail_argument_checks(lib):
     assert n >= f + 2 * 4096 * 8 * 1024 * 2 and n % 256 == 0
 
 
+def test_topk_argument_checks(lib):
+    def call(scores=16, stride=8, rows=2, L=8, k=4, offset=0, out=16):
+        return lib.sa_topk_indices(scores, stride, rows, L, k, offset, out, None)
+    assert call(stride=4) == INVALID              # rows overlap
+    assert call(scores=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(out=2) == INVALID                 # 4-byte alignment
+    assert call(offset=-1) == INVALID
+    assert call(L=-1) == INVALID
+    assert call(rows=0) == OK                     # nothing to do, nothing touched
+    assert call(k=0) == OK
+
+
 def test_workspace_size_queries(lib):
     # without a device the size falls back to one SM; it is always >= 256, 256-aligned
     for B, T, K in [(1, 16, 192), (64, 1, 640), (1, 8192, 640), (0, 0, 0)]:

@@ -308,3 +308,30 @@ def test_block_tail_workload_sampled():
     # wo_b's outputs reach several units: each may also differ by 2^-7 of its magnitude
     # (its own bf16 rounding is 2^-9)
     compare(got, zref, "block_tail", per_value=True)
+
+
+@pytest.mark.parametrize("rows,L,k,mode", [
+    (256, 4096, 512, "causal"),   # prefill-like: the visible prefix grows row by row
+    (64, 4096, 512, "full"),      # decode-like
+    (8, 65536, 512, "full"),      # long context: keys re-read from L2 on every pass
+    (32, 1000, 512, "ties"),      # many equal scores: ties go to the smaller position
+    (16, 300, 512, "masked"),     # NaN and -inf, fewer than k positions to choose
+    (4, 0, 16, "empty"),          # no positions at all
+])
+def test_topk_matches_oracle(rows, L, k, mode):
+    """The top-k selection is exact: the same int32 positions, in the same
+    order, as the oracle's sort."""
+    g = torch.Generator().manual_seed(rows * 7 + L)
+    s = torch.randn(rows, L, generator=g)
+    if mode == "causal":
+        for r in range(rows):
+            s[r, (r * L) // rows + 1:] = float("-inf")
+    elif mode == "ties":
+        s = torch.round(s * 4) / 4
+    elif mode == "masked":
+        s[torch.rand(rows, L, generator=g) < 0.1] = float("nan")
+        s[torch.rand(rows, L, generator=g) < 0.2] = float("-inf")
+    got = sa.topk_indices(s.cuda(), k, offset=128)
+    torch.cuda.synchronize()
+    ref = oracle.topk_indices(s.numpy(), k, offset=128)
+    assert np.array_equal(got.cpu().numpy(), ref)

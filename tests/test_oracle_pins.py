@@ -373,3 +373,53 @@ def test_wo_b_equals_one_group_wo_a_and_a_hand_case():
     yh = np.array([[1.0, 2.0], [3.0, 4.0]])
     Wh = bf16([[1.0, 0.5], [-2.0, 0.25]])
     assert np.array_equal(oracle.wo_b(yh, Wh), np.array([[2.0, -1.5], [5.0, -5.0]]))
+
+
+# ------------------------------------------------------------------ top-k selection
+
+def _topk_brute(row, k, offset):
+    """Pick the largest remaining score k times (smaller position on ties)."""
+    left = [(j, x) for j, x in enumerate(row) if not (math.isnan(x) or x == -math.inf)]
+    chosen = []
+    for _ in range(min(k, len(left))):
+        best = max(left, key=lambda jx: (jx[1], -jx[0]))
+        chosen.append(best[0])
+        left.remove(best)
+    chosen.sort()
+    return [j + offset for j in chosen] + [-1] * (k - len(chosen))
+
+
+def test_topk_brute_force_with_ties_and_masks():
+    rng = np.random.default_rng(21)
+    for trial in range(40):
+        L, k = int(rng.integers(0, 30)), int(rng.integers(1, 12))
+        row = np.round(rng.standard_normal(L), 1)          # many ties
+        row[rng.random(L) < 0.2] = -np.inf
+        row[rng.random(L) < 0.05] = np.nan
+        got = oracle.topk_indices(row[None, :], k, offset=7)[0].tolist()
+        assert got == _topk_brute(row.tolist(), k, 7), (trial, row, k)
+
+
+def test_topk_defining_property():
+    """Every chosen score is at least every score left out; as many positions
+    as can be chosen; ascending; offset applied; -1 after them."""
+    rng = np.random.default_rng(22)
+    scores = rng.standard_normal((6, 500)).astype(np.float32)
+    for r in range(6):
+        scores[r, 400 - 60 * r:] = -np.inf                 # causal-style masked tails
+    k = 256
+    got = oracle.topk_indices(scores, k, offset=128)
+    for r in range(6):
+        valid = np.nonzero(np.isfinite(scores[r]))[0]
+        sel = got[r][got[r] >= 0] - 128
+        assert sel.size == min(k, valid.size)
+        assert np.all(np.diff(sel) > 0) and np.all(got[r][sel.size:] == -1)
+        rest = np.setdiff1d(valid, sel)
+        if rest.size and sel.size:
+            assert scores[r, sel].min() >= scores[r, rest].max()
+
+
+def test_topk_signed_zeros_tie():
+    """-0.0 and +0.0 compare equal, so they tie and the smaller position wins."""
+    row = np.array([1.0, -0.0, 0.0, -0.0, 2.0])
+    assert oracle.topk_indices(row[None, :], 3)[0].tolist() == [0, 1, 4]
