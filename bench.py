@@ -412,6 +412,49 @@ def bench_topk(steps: int, warmup: int, dev, pk: dict) -> dict:
                          "frac": gbs / pk["hbm_gbs"], "peak_note": f"{pk['source']} HBM copy"}}
 
 
+def bench_decode_fp4(steps: int, warmup: int, dev, pk: dict) -> dict:
+    """The decode workload with its compressed cache stored as fp4 (e2m1 codes
+    and an E4M3 scale per 16 features, 288 bytes per row) next to the bf16
+    window: the same lists, the two-source fp4 call, rotating input sets larger
+    than L2."""
+    import sparse_latent_attention_02_gb300 as sa
+    wl = I.WORKLOADS["decode"]
+    D = wl.D
+    n_sets = 4
+    sets = []
+    for i in range(n_sets):
+        x = I.make_inputs(wl, seed=200 + i, device=dev)
+        g = torch.Generator(device=dev).manual_seed(300 + i)
+        codes = torch.randint(0, 256, (wl.B, wl.C, D // 2), generator=g, device=dev,
+                              dtype=torch.int32).to(torch.uint8)
+        scales = (0x20 + torch.randint(0, 8, (wl.B, wl.C, D // 16), generator=g, device=dev,
+                                       dtype=torch.int32)).to(torch.uint8)
+        win = x["kv"][:, :wl.W].contiguous()
+        out = torch.empty((wl.B, wl.T, wl.H, D), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(sa.workspace_size(wl.B, wl.T, wl.K), dtype=torch.uint8, device=dev)
+        sets.append((x, win, codes, scales, out, ws))
+        del x["kv"]
+    fns = [lambda x=x, win=win, c=c, sc=sc, o=o, ws=ws: sa.sparse_attn_two_source_fp4(
+        x["q"], win, c, sc, x["sink"], x["idx"], wl.scale, out=o, workspace=ws)
+        for x, win, c, sc, o, ws in sets]
+    secs, _ = time_graph_steps(fns, steps, warmup)
+    for *_, ws in sets:
+        sa.check_errors(ws)
+    step_s = secs / steps
+    idx = sets[0][0]["idx"]
+    win_rows = int(((idx >= 0) & (idx < wl.W)).sum())
+    fp4_rows = int((idx >= wl.W).sum())
+    nbytes = (win_rows * D * 2 + fp4_rows * (D // 2 + D // 16) + wl.n_queries * wl.H * D * 4
+              + idx.numel() * 4 + wl.H * 4)
+    gbs = nbytes / step_s / 1e9
+    return {"workload": f"decode with fp4 compressed rows: B={wl.B} K={wl.K} ({wl.W} bf16 window + "
+                        f"{wl.C} fp4 compressed rows per batch row)",
+            "ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "gbs": gbs,
+            "bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "peak_note": f"{pk['source']} HBM copy"}}
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
     """The fp64 oracle, as it stands, on the host cores: whole decode steps
     (all queries of one input set) repeated until about `budget_s` seconds."""
@@ -475,6 +518,7 @@ def run_ours(args):
                                  "peak_note": f"{pk['source']} HBM copy"}
             extra[name] = r
         extra["topk"] = bench_topk(max(3, min(args.steps, 50)), max(args.warmup, 3), dev, pk)
+        extra["decode_fp4"] = bench_decode_fp4(max(3, min(args.steps, 200)), max(args.warmup, 3), dev, pk)
     sampler.stop()
     e2e = head.pop("e2e", None)
     cpu = (cpu_baseline(args.workload, budget_s=args.cpu_seconds)

@@ -119,6 +119,33 @@ sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W,
                                     void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * sa_sparse_attn_two_source with the compressed cache stored as fp4: the
+ * "DeepSeek-V4.1 > 40 layers" page quantizes each compressed latent to fp4 in
+ * groups of 16 with an E4M3 scale per group (`fp4_act_quant(latent, 16, True,
+ * scale_dtype=torch.float8_e4m3fn)`) before caching it, so its values lie on
+ * that grid and this packed form holds them exactly in 288 bytes per row
+ * instead of 1024.  The kernel decodes each gathered row into bf16 in shared
+ * memory; the result is the same as sa_sparse_attn_two_source on the decoded
+ * cache.
+ *   codes  uint8, row v - W of batch element b at codes + (b * compressed_bstride
+ *          + v - W) * D/2: byte i holds feature 2i in its low nibble and 2i+1 in
+ *          its high nibble, each an e2m1 code (bit 3 sign, bits 2..0 index the
+ *          magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6); 16-byte aligned
+ *   scales uint8, at scales + (b * compressed_bstride + v - W) * D/16 + g: the
+ *          E4M3 scale (bias 7, no infinities, S.1111.111 = NaN) of features
+ *          16g .. 16g+15
+ *   compressed_bstride  batch stride of both, in rows (>= C)
+ * Other arguments as for sa_sparse_attn_two_source; the window source stays bf16.
+ */
+sa_status sa_sparse_attn_two_source_fp4(const void *q, const void *window_kv, int W,
+                                        int64_t window_bstride, const uint8_t *codes,
+                                        const uint8_t *scales, int C,
+                                        int64_t compressed_bstride, const float *sink,
+                                        const int32_t *idx, float scale, int B, int T,
+                                        int H, int D, int K, void *out, sa_dtype out_dtype,
+                                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Bytes of workspace `sa_sparse_attn_rope_wo_a` needs: the attention
  * workspace plus the bf16 attention output [B, T, H, D] it keeps between the
  * two steps.

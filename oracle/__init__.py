@@ -146,6 +146,57 @@ def sparse_attn_two_source(q, window_kv, W: int, compressed_kv, C: int, sink, id
     return sparse_attn(qb, np.ascontiguousarray(kv), sink, idx, scale, queries=queries, n_threads=n_threads)
 
 
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def e4m3_values(b) -> np.ndarray:
+    """OCP FP8 E4M3 ("fn": bias 7, no infinities, S.1111.111 = NaN) bytes -> fp64."""
+    b = np.asarray(b, dtype=np.int64)
+    e, m = (b >> 3) & 15, b & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return np.where(b & 0x80, -v, v)
+
+
+def dequant_fp4(codes, scales) -> np.ndarray:
+    """fp4 compressed rows (the "DeepSeek-V4.1 > 40 layers" page's
+    `fp4_act_quant(latent, 16, True, scale_dtype=torch.float8_e4m3fn)`: e2m1
+    values in groups of 16 features with an E4M3 scale each) -> fp64 values.
+    codes uint8 [..., D/2]: byte i = feature 2i (low nibble), 2i+1 (high);
+    e2m1 code: bit 3 sign, bits 2..0 index the magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6.
+    scales uint8 [..., D/16]: E4M3 scale of features 16g .. 16g+15."""
+    c = np.asarray(codes, dtype=np.uint8)
+    nib = np.stack([c & 15, c >> 4], axis=-1).reshape(*c.shape[:-1], 2 * c.shape[-1]).astype(np.int64)
+    mag = np.asarray(E2M1_MAGNITUDES)[nib & 7]
+    val = np.where(nib & 8, -mag, mag)
+    sc = np.repeat(e4m3_values(scales), 16, axis=-1)
+    return val * sc
+
+
+def bf16_bits_exact(x) -> np.ndarray:
+    """fp64 values that bf16 holds exactly -> bf16 bit patterns (uint16)."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    if not np.array_equal(f.astype(np.float64), np.asarray(x, dtype=np.float64), equal_nan=True):
+        raise ValueError("value not representable in fp32")
+    u = f.view(np.uint32)
+    if np.any(u & 0xFFFF):
+        raise ValueError("value not representable in bf16")
+    return (u >> 16).astype(np.uint16)
+
+
+def sparse_attn_two_source_fp4(q, window_kv, W: int, codes, scales, C: int, sink, idx, scale: float,
+                               queries=None, n_threads: int = 0):
+    """sparse_attn_two_source with the compressed rows given as fp4: they are
+    decoded (exactly, into bf16) and the two sources concatenated."""
+    qb = _as_bf16_bits(q)
+    B = qb.shape[0]
+    comp = None
+    if C:
+        comp = bf16_bits_exact(dequant_fp4(np.asarray(codes)[:B, :C], np.asarray(scales)[:B, :C]))
+    return sparse_attn_two_source(qb, window_kv, W, comp, C, sink, idx, scale, queries=queries,
+                                  n_threads=n_threads)
+
+
 def topk_indices(scores, k: int, offset: int = 0) -> np.ndarray:
     """Top-k selection of compressed positions (the "DeepSeek-V4.1 > 40 layers"
     page's `_compress_topk_idxs`: int32 positions offset by the window length,

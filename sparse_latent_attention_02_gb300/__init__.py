@@ -18,7 +18,8 @@ import torch
 
 from ._build import LIB as _LIB_PATH, build  # noqa: F401
 
-__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_rope_wo_a", "sparse_attn_block_tail",
+__all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_two_source_fp4", "sparse_attn_rope_wo_a",
+           "sparse_attn_block_tail",
            "topk_indices", "rope_table", "workspace_size",
            "fused_workspace_size", "check_errors", "SAError", "library", "build"]
 
@@ -29,7 +30,7 @@ EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_tw
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
            "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail",
-           "sa_topk_indices")
+           "sa_topk_indices", "sa_sparse_attn_two_source_fp4")
 
 
 class SAError(RuntimeError):
@@ -72,6 +73,9 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_sparse_attn_block_tail.restype = I
             lib.sa_sparse_attn_block_tail.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
                                                       V, I, V, V, Z, V]
+            lib.sa_sparse_attn_two_source_fp4.restype = I
+            lib.sa_sparse_attn_two_source_fp4.argtypes = [V, V, I, L, V, V, I, L, V, V, F, I, I, I, I, I,
+                                                          V, I, V, Z, V]
             lib.sa_topk_indices.restype = I
             lib.sa_topk_indices.argtypes = [V, ctypes.c_int64, ctypes.c_int64, I, I, I, V, V]
             lib.sa_rope_table.restype = I
@@ -244,6 +248,65 @@ def sparse_attn_two_source(q: torch.Tensor, window_kv: torch.Tensor | None,
                                          workspace.numel() * workspace.element_size(),
                                          _stream_ptr(stream))
     _check(code, "sa_sparse_attn_two_source")
+    if check:
+        check_errors(workspace, stream)
+    return out
+
+
+def sparse_attn_two_source_fp4(q: torch.Tensor, window_kv: torch.Tensor | None,
+                               codes: torch.Tensor | None, scales: torch.Tensor | None,
+                               sink: torch.Tensor, idx: torch.Tensor, scale: float,
+                               W: int | None = None, C: int | None = None,
+                               out: torch.Tensor | None = None,
+                               out_dtype: torch.dtype = torch.bfloat16,
+                               workspace: torch.Tensor | None = None, stream=None,
+                               check: bool = False) -> torch.Tensor:
+    """sparse_attn_two_source with the compressed cache as fp4: codes uint8
+    [Bmax, >= C, 256] (two e2m1 codes per byte, low nibble first) and scales
+    uint8 [Bmax, >= C, 32] (E4M3, one per 16 features); the window stays bf16."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(sink, "sink", torch.float32, 1)
+    _need(idx, "idx", torch.int32, 3)
+    B, T, H, D = q.shape
+    if sink.shape[0] != H or idx.shape[:2] != (B, T):
+        raise ValueError("sink / idx shapes do not match q")
+    pw, W, sw = _source(window_kv, "window_kv", W, B, D)
+    if codes is None or scales is None:
+        if C:
+            raise ValueError("codes and scales are needed when C > 0")
+        pc = ps = 0
+        C, sc = 0, 0
+    else:
+        for t, name, width in ((codes, "codes", D // 2), (scales, "scales", D // 16)):
+            if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or t.dim() != 3 or t.shape[2] != width:
+                raise TypeError(f"{name} must be a uint8 tensor [batch, rows, {width}]")
+            if not t.is_cuda and not t.is_pinned():
+                raise ValueError(f"{name} must live on a CUDA device or in page-locked host memory")
+            if t.stride(2) != 1 or t.stride(1) != width or t.shape[0] < B:
+                raise ValueError(f"{name} must have contiguous rows and >= {B} batch rows")
+        if codes.shape[:2] != scales.shape[:2] or codes.stride(0) // (D // 2) != scales.stride(0) // (D // 16):
+            raise ValueError("codes and scales must have the same rows and batch stride")
+        C = codes.shape[1] if C is None else int(C)
+        if not 0 <= C <= codes.shape[1]:
+            raise ValueError(f"{C} rows used of {codes.shape[1]}")
+        pc, ps, sc = codes.data_ptr(), scales.data_ptr(), codes.stride(0) // (D // 2)
+    K = idx.shape[2]
+    if out is None:
+        out = torch.empty((B, T, H, D), dtype=out_dtype, device=q.device)
+    else:
+        _need(out, "out", out.dtype, 4)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bf16 or fp32")
+    lib = library()
+    need = int(lib.sa_sparse_attn_workspace_size(B, T, H, D, K))
+    if workspace is None:
+        workspace = _workspace(need, q.device, "attn")
+    code = lib.sa_sparse_attn_two_source_fp4(q.data_ptr(), pw, W, sw, pc, ps, C, sc, sink.data_ptr(),
+                                             idx.data_ptr(), float(scale), B, T, H, D, K, out.data_ptr(),
+                                             1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
+                                             workspace.numel() * workspace.element_size(),
+                                             _stream_ptr(stream))
+    _check(code, "sa_sparse_attn_two_source_fp4")
     if check:
         check_errors(workspace, stream)
     return out

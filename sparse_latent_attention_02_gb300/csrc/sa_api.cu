@@ -77,6 +77,8 @@ struct KvSources {
     int W;
     const void *kv2;
     int64_t kv2_bstride;
+    const void *codes = nullptr;    // source 1 in fp4 instead of kv2: e2m1 codes and E4M3 scales
+    const void *scales = nullptr;
 };
 
 sa_status fill_attn_params(AttnParams &p, const void *q, const KvSources &src, const float *sink,
@@ -95,10 +97,22 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const KvSources &src, c
             if (st != SA_OK)
                 return st;
         }
-        if (N > src.W) {
+        if (N > src.W && !src.codes) {
             const sa_status st = resolve_kv(src.kv2, &dev_kv2, &host_kv2);
             if (st != SA_OK)
                 return st;
+        }
+        if (N > src.W && src.codes) {
+            const void *c = nullptr, *sc = nullptr;
+            bool hc = false, hs = false;
+            sa_status st = resolve_kv(src.codes, &c, &hc);
+            if (st == SA_OK)
+                st = resolve_kv(src.scales, &sc, &hs);
+            if (st != SA_OK)
+                return st;
+            p.kv2_codes = static_cast<const uint8_t *>(c);
+            p.kv2_scales = static_cast<const uint8_t *>(sc);
+            host_kv2 = hc || hs;
         }
     }
     // warm L2 with upcoming rows only when kv lives in device memory too large
@@ -250,18 +264,17 @@ sa_status sa_sparse_attn(const void *q, const void *kv, const float *sink, const
     return launch_attention(p, sch, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
 }
 
-sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W, int64_t window_bstride,
-                                    const void *compressed_kv, int C, int64_t compressed_bstride,
-                                    const float *sink, const int32_t *idx, float scale, int B, int T, int H,
-                                    int D, int K, void *out, sa_dtype out_dtype, void *workspace,
-                                    size_t ws_bytes, void *stream)
+// Shared by the two-source entry points: checks, then one launch.
+static sa_status two_source_call(const void *q, const KvSources &src, int C, const float *sink, const int32_t *idx,
+                          float scale, int B, int T, int H, int D, int K, void *out, sa_dtype out_dtype,
+                          void *workspace, size_t ws_bytes, void *stream)
 {
+    const int W = src.W;
     if (W < 0 || C < 0 || (int64_t)W + C >= ((int64_t)1 << 31))
         return SA_ERR_INVALID_ARG;
     const int N = W + C;
-    // the sources' own checks; kv itself is checked per source below
-    sa_status st = check_attn_args(q, W > 0 ? window_kv : compressed_kv, sink, idx, scale, B, T, H, D, N, K,
-                                   out, workspace);
+    const void *any_src = W > 0 ? src.kv : (src.codes ? src.codes : src.kv2);
+    sa_status st = check_attn_args(q, any_src, sink, idx, scale, B, T, H, D, N, K, out, workspace);
     if (st != SA_OK)
         return st;
     if (out_dtype != SA_BF16 && out_dtype != SA_F32)
@@ -270,12 +283,16 @@ sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W,
     if (BT == 0)
         return SA_OK;
     if (K > 0) {
-        if (W > 0 && (!window_kv || !aligned(window_kv, 16) || window_bstride < W))
+        if (W > 0 && (!src.kv || !aligned(src.kv, 16) || src.kv_bstride < W))
             return SA_ERR_INVALID_ARG;
-        if (C > 0 && (!compressed_kv || !aligned(compressed_kv, 16) || compressed_bstride < C))
-            return SA_ERR_INVALID_ARG;
-        if ((int64_t)B * (W > 0 ? window_bstride : 0) >= ((int64_t)1 << 40) ||
-            (int64_t)B * (C > 0 ? compressed_bstride : 0) >= ((int64_t)1 << 40))
+        if (C > 0) {
+            if (src.kv2_bstride < C)
+                return SA_ERR_INVALID_ARG;
+            if (src.codes ? (!aligned(src.codes, 16) || !src.scales) : (!src.kv2 || !aligned(src.kv2, 16)))
+                return SA_ERR_INVALID_ARG;
+        }
+        if ((int64_t)B * (W > 0 ? src.kv_bstride : 0) >= ((int64_t)1 << 40) ||
+            (int64_t)B * (C > 0 ? src.kv2_bstride : 0) >= ((int64_t)1 << 40))
             return SA_ERR_UNSUPPORTED;
     }
     int sms = 0;
@@ -288,12 +305,37 @@ sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W,
     if (K == 0)
         return cudaMemsetAsync(out, 0, (size_t)BT * H * D * esz, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
     AttnParams p;
-    const KvSources src{window_kv, window_bstride, W, compressed_kv, compressed_bstride};
     st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
     if (st != SA_OK)
         return st;
     const Schedule sch = attn_schedule(BT, K, sms);
     return launch_attention(p, sch, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
+sa_status sa_sparse_attn_two_source(const void *q, const void *window_kv, int W, int64_t window_bstride,
+                                    const void *compressed_kv, int C, int64_t compressed_bstride,
+                                    const float *sink, const int32_t *idx, float scale, int B, int T, int H,
+                                    int D, int K, void *out, sa_dtype out_dtype, void *workspace,
+                                    size_t ws_bytes, void *stream)
+{
+    const KvSources src{window_kv, window_bstride, W, compressed_kv, compressed_bstride};
+    return two_source_call(q, src, C, sink, idx, scale, B, T, H, D, K, out, out_dtype, workspace, ws_bytes,
+                           stream);
+}
+
+sa_status sa_sparse_attn_two_source_fp4(const void *q, const void *window_kv, int W, int64_t window_bstride,
+                                        const uint8_t *codes, const uint8_t *scales, int C,
+                                        int64_t compressed_bstride, const float *sink, const int32_t *idx,
+                                        float scale, int B, int T, int H, int D, int K, void *out,
+                                        sa_dtype out_dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (C > 0 && (!codes || !scales))
+        return SA_ERR_INVALID_ARG;
+    KvSources src{window_kv, window_bstride, W, nullptr, compressed_bstride};
+    src.codes = C > 0 ? codes : nullptr;
+    src.scales = C > 0 ? scales : nullptr;
+    return two_source_call(q, src, C, sink, idx, scale, B, T, H, D, K, out, out_dtype, workspace, ws_bytes,
+                           stream);
 }
 
 size_t sa_sparse_attn_rope_wo_a_workspace_size(int B, int T, int H, int D, int K, int G, int R)

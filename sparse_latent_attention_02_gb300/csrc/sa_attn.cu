@@ -219,14 +219,14 @@ __device__ __forceinline__ int compact_staged(const int32_t *raw, int len, int N
 
 // Warm L2 with latent rows (whole warp, one line prefetch per 128 bytes):
 // rows list[j0 .. j1) of batch element bidx, skipping entries outside [0, N).
-template <bool TWO>
+template <bool TWO, bool FP4>
 __device__ __forceinline__ void prefetch_rows(const AttnParams &p, int64_t bidx, const int32_t *list, int j0,
                                               int j1, int lane)
 {
     // lane = 8 * (row within a group of 4) + line
     for (int j = j0 + (lane >> 3); j < j1; j += 4) {
         const int v = list[j];
-        if (v >= 0 && v < p.N)
+        if (v >= 0 && v < p.N && !(FP4 && v >= p.W))   // fp4 rows: no bf16 row to warm
             prefetch_l2_line(reinterpret_cast<const uint8_t *>(kv_row<TWO>(p, bidx, v)) + (lane & 7) * 128);
     }
 }
@@ -298,7 +298,7 @@ __device__ __forceinline__ bool load_q(const AttnParams &p, uint32_t sbase, cons
 // staging buffer, compacts the list into a double-buffered shared list and
 // publishes its length.  When kv is larger than L2 it then warms L2 with the
 // next segment's rows while the current segment is processed.
-template <bool TWO>
+template <bool TWO, bool FP4>
 __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int lane,
                              volatile int *abort_flag)
 {
@@ -352,7 +352,7 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
             if (p.prefetch_rows) {
                 cp_async_wait_all();
                 __syncwarp();
-                prefetch_rows<TWO>(p, sn.q / p.T, raw, 0, sn.j1 - sn.j0, lane);
+                prefetch_rows<TWO, FP4>(p, sn.q / p.T, raw, 0, sn.j1 - sn.j0, lane);
             }
             s = sn;
         }
@@ -364,13 +364,50 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     __syncwarp();
 }
 
+// OCP FP8 E4M3 (the "fn" variant: bias 7, no infinities, S.1111.111 is NaN).
+__device__ __forceinline__ float e4m3_value(uint32_t b)
+{
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    float v;
+    if (e == 0u)
+        v = (float)m * 0.001953125f;                        // m * 2^-9
+    else if (e == 15u && m == 7u)
+        v = __uint_as_float(0x7fc00000u);                   // NaN
+    else
+        v = __uint_as_float(((e + 120u) << 23) | (m << 20));   // (1 + m/8) * 2^(e-7)
+    return (b & 0x80u) ? -v : v;
+}
+
+// Eight e2m1 codes (nibble k of `codes` = feature k: bit 3 sign, bits 2..0 the
+// magnitude index into 0, 0.5, 1, 1.5, 2, 3, 4, 6) times their group's scale,
+// as four packed bf16 pairs (exact: a code times an E4M3 scale has at most
+// five significant bits).
+__device__ __forceinline__ uint4 dequant_e2m1x8(uint32_t codes, float scale)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        float v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t c = (codes >> (4 * (k + h))) & 15u, i = c & 7u;
+            // twice the magnitude: 0, 1, 2, 3, 4, 6, 8, 12
+            const uint32_t twice = i < 4u ? i : (2u + (i & 1u)) << ((i >> 1) - 1u);
+            const float mag = (float)twice * 0.5f * scale;
+            v[h] = (c & 8u) ? -mag : mag;
+        }
+        w[k >> 1] = pack_bf16x2(v[0], v[1]);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Warps 8-23: gather the compacted rows, chunk by chunk, in two groups of
 // eight warps: group g fills tiles g and g + 2 (a tile is two 64-feature
 // slices of the 128 rows), so all four tiles of a chunk can be in flight at
 // once and each tile is refilled as soon as the PV product frees it.  Warp w
 // of a group copies rows 16w .. 16w+15; rows past the end of the list are
 // zero-filled.
-template <bool TWO>
+template <bool TWO, bool FP4>
 __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, int gi, int lane,
                             volatile int *abort_flag)
 {
@@ -416,12 +453,51 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                 if (!ok)
                     break;
                 const int sl = 2 * d + (pc >> 3), ch = pc & 7;
+                if constexpr (!FP4) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + 2 * i;
-                    const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r * 128 + ((ch ^ (r & 7)) << 4);
-                    const uint16_t *src = row_ptr(row[i] < 0 ? 0 : row[i]) + sl * 64 + ch * 8;
-                    cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = r0 + 2 * i;
+                        const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r * 128 + ((ch ^ (r & 7)) << 4);
+                        const uint16_t *src = row_ptr(row[i] < 0 ? 0 : row[i]) + sl * 64 + ch * 8;
+                        cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
+                    }
+                } else {
+                    // window rows (and empty slots) by cp.async; compressed rows are
+                    // fp4: eight features = four code bytes and their group's scale,
+                    // loaded for four rows at a time, then decoded into the slot
+                    const int f0 = sl * 64 + ch * 8;
+#pragma unroll
+                    for (int h = 0; h < 8; h += 4) {
+                        uint32_t code[4], scb[4];
+#pragma unroll
+                        for (int i = h; i < h + 4; ++i) {
+                            const int v = row[i];
+                            code[i - h] = 0u;
+                            scb[i - h] = 0u;
+                            if (v >= p.W) {
+                                const size_t cr = (size_t)bidx * (size_t)p.kv2_bstride + (size_t)(v - p.W);
+                                code[i - h] = __ldg(reinterpret_cast<const uint32_t *>(p.kv2_codes + cr * (D / 2) + f0 / 2));
+                                scb[i - h] = __ldg(p.kv2_scales + cr * (D / 16) + f0 / 16);
+                            } else {
+                                const int r = r0 + 2 * i;
+                                const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r * 128 + ((ch ^ (r & 7)) << 4);
+                                // an empty slot copies nothing; its source is any valid row
+                                const uint16_t *src =
+                                    v >= 0 ? kvb + (size_t)v * D + f0
+                                           : (p.W > 0 ? kvb : reinterpret_cast<const uint16_t *>(p.kv2_codes));
+                                cp_async16(dst, src, v < 0 ? 0u : 16u);
+                            }
+                        }
+#pragma unroll
+                        for (int i = h; i < h + 4; ++i) {
+                            if (row[i] >= p.W) {
+                                const int r = r0 + 2 * i;
+                                uint4 *dst = reinterpret_cast<uint4 *>(smem + OFF_KV + sl * SLICE_BYTES + r * 128 +
+                                                                       ((ch ^ (r & 7)) << 4));
+                                *dst = dequant_e2m1x8(code[i - h], e4m3_value(scb[i - h]));
+                            }
+                        }
+                    }
                 }
                 cp_async_commit();
             }
@@ -443,7 +519,7 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
             // does not wait for HBM
             if (p.prefetch_rows && c + 1 < nc) {
                 const int j = (c + 1) * CH + ROWS_PER_GATHER_WARP * wg + (lane >> 1);
-                if (j < n) {
+                if (j < n && !(FP4 && cidx[j] >= p.W)) {
                     const uint8_t *rp = reinterpret_cast<const uint8_t *>(row_ptr(cidx[j])) +
                                         (grp + 2 * (lane & 1)) * 256;
                     prefetch_l2_line(rp);
@@ -988,7 +1064,7 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     }
 }
 
-template <bool TWO>
+template <bool TWO, bool FP4>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant__ AttnParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -1044,12 +1120,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         softmax_role(p, smem, sbase, tmem, warp, lane, abort_flag);
     } else if (warp < WARP_GATHER0 + NUM_GATHER_WARPS) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_GATHER) : "memory");
-        gather_role<TWO>(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
+        gather_role<TWO, FP4>(p, smem, sbase, warp - WARP_GATHER0, lane, abort_flag);
     } else {
         // the last warpgroup: control warp, MMA warp and two warps without a role
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LAST) : "memory");
         if (warp == WARP_CONTROL)
-            control_role<TWO>(p, smem, sbase, lane, abort_flag);
+            control_role<TWO, FP4>(p, smem, sbase, lane, abort_flag);
         else if (warp == WARP_MMA && lane == 0)
             mma_role(p, smem, sbase, tmem, abort_flag);
     }
@@ -1115,9 +1191,11 @@ size_t attn_workspace_bytes(int64_t BT, int K, int num_sms)
 
 cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
 {
-    // the two-source build only when a second source is in use
-    const bool two = p.kv2 != nullptr && p.W < p.N;
-    void (*kernel)(AttnParams) = two ? attn::attn_kernel<true> : attn::attn_kernel<false>;
+    // the two-source builds only when a second source is in use
+    const bool second = p.W < p.N;
+    void (*kernel)(AttnParams) = second && p.kv2_codes ? attn::attn_kernel<true, true>
+                                 : second && p.kv2  ? attn::attn_kernel<true, false>
+                                                    : attn::attn_kernel<false, false>;
     cudaError_t ea = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)attn::SMEM_BYTES);
     if (ea != cudaSuccess)

@@ -25,6 +25,10 @@ struct AttnParams {
     const uint16_t *kv2;
     int64_t kv_bstride, kv2_bstride;
     int W;
+    // source 1 in fp4 instead (kv2 unused): per row D/2 bytes of e2m1 codes
+    // and D/16 E4M3 scales, same batch stride in rows
+    const uint8_t *kv2_codes;
+    const uint8_t *kv2_scales;
     const int32_t *idx;        // int32 [B*T, K]
     const float *sink;         // fp32 [H]
     void *out;                 // [B*T, H, D] bf16 or fp32

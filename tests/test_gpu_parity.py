@@ -335,3 +335,44 @@ def test_topk_matches_oracle(rows, L, k, mode):
     torch.cuda.synchronize()
     ref = oracle.topk_indices(s.numpy(), k, offset=128)
     assert np.array_equal(got.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("B,T,K,W,C,host_c", [
+    (4, 1, 640, 128, 4096, False),    # decode shape, split schedule
+    (1, 40, 300, 128, 600, False),    # whole queries per CTA
+    (2, 3, 200, 0, 500, False),       # fp4 rows only
+    (3, 2, 256, 128, 900, True),      # fp4 cache in page-locked host memory
+])
+def test_two_source_fp4_matches_decoded_cache(B, T, K, W, C, host_c):
+    """Compressed rows stored as fp4 (e2m1 codes, an E4M3 scale per 16
+    features) give exactly the result of the bf16 call on the decoded cache,
+    and match the oracle.  Scale padding is E4M3 NaN: reading any row past C,
+    or a spare batch row, would show in the output."""
+    g = torch.Generator().manual_seed(B * 31 + C)
+    D = 512
+    nan_bf16 = float("nan")
+    win = torch.full((B + 1, W + 8, D), nan_bf16, dtype=torch.bfloat16)
+    win[:B, :W] = I.rms_rows(torch.randn(B, W, D, generator=g)).to(torch.bfloat16)
+    codes = torch.randint(0, 256, (B + 1, C + 16, D // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+    scales = torch.full((B + 1, C + 16, D // 16), 0x7F, dtype=torch.uint8)
+    # positive scales in [0.25, 0.47): with codes drawn uniformly the decoded
+    # rows have an RMS near 1, like the RMS-normalised latents they stand for
+    scales[:B, :C] = (0x20 + torch.randint(0, 8, (B, C, D // 16), generator=g)).to(torch.uint8)
+    q = torch.randn(B, T, 64, D, generator=g).to(torch.bfloat16)
+    sink = torch.randn(64, generator=g)
+    idx = torch.randint(0, W + C, (B, T, K), generator=g, dtype=torch.int32)
+    idx[torch.rand(B, T, K, generator=g) < 0.1] = -1
+    gd = to_dev(dict(q=q, sink=sink, idx=idx))
+    win_d = win.cuda() if W else None
+    place = (lambda t: t.pin_memory()) if host_c else (lambda t: t.cuda())
+    got = sa.sparse_attn_two_source_fp4(gd["q"], win_d, place(codes), place(scales), gd["sink"], gd["idx"],
+                                        512 ** -0.5, W=W, C=C, out_dtype=torch.float32, check=True)
+    decoded = torch.from_numpy(oracle.bf16_bits_exact(
+        oracle.dequant_fp4(codes[:B, :C].numpy(), scales[:B, :C].numpy())).view(np.int16)).view(torch.bfloat16)
+    ref16 = sa.sparse_attn_two_source(gd["q"], win_d, decoded.cuda(), gd["sink"], gd["idx"], 512 ** -0.5,
+                                      W=W, C=C, out_dtype=torch.float32, check=True)
+    assert torch.equal(got, ref16)
+    ref, bad = oracle.sparse_attn_two_source_fp4(q, win, W, codes.numpy(), scales.numpy(), C, sink, idx,
+                                                 512 ** -0.5)
+    assert bad == 0
+    compare(got.double().cpu().numpy(), ref, f"fp4 two sources B{B} W{W} C{C}")

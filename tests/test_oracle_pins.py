@@ -423,3 +423,40 @@ def test_topk_signed_zeros_tie():
     """-0.0 and +0.0 compare equal, so they tie and the smaller position wins."""
     row = np.array([1.0, -0.0, 0.0, -0.0, 2.0])
     assert oracle.topk_indices(row[None, :], 3)[0].tolist() == [0, 1, 4]
+
+
+# ------------------------------------------------------------------ fp4 compressed rows
+
+def test_e2m1_codes_and_nibble_order():
+    """The 16 e2m1 codes decode to +-{0, .5, 1, 1.5, 2, 3, 4, 6} (OCP MX
+    element values); byte i holds feature 2i in its low nibble."""
+    codes = np.array([[0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE]], dtype=np.uint8)
+    scales = np.array([[0x38]], dtype=np.uint8)            # 1.0
+    got = oracle.dequant_fp4(codes, scales)[0]
+    want = [0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6]
+    assert np.array_equal(got, np.array(want))
+
+
+@pytest.mark.parametrize("byte,value", [(0x38, 1.0), (0xB8, -1.0), (0x7E, 448.0), (0x08, 2.0 ** -6),
+                                        (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0x00, 0.0),
+                                        (0x40, 2.0), (0x3C, 1.5)])
+def test_e4m3_known_bytes(byte, value):
+    assert oracle.e4m3_values(byte) == value
+
+
+def test_e4m3_nan_and_scale_applies_per_group():
+    assert np.isnan(oracle.e4m3_values(0x7F)) and np.isnan(oracle.e4m3_values(0xFF))
+    codes = np.full((1, 16), 0x22, dtype=np.uint8)          # every feature code 2 = 1.0
+    scales = np.array([[0x38, 0x40]], dtype=np.uint8)       # groups: 1.0, 2.0
+    got = oracle.dequant_fp4(codes, scales)[0]
+    assert np.array_equal(got, np.r_[np.ones(16), 2 * np.ones(16)])
+
+
+def test_fp4_values_are_exact_in_bf16():
+    """Every code times every finite E4M3 scale is a bf16 value (so the GPU's
+    bf16 decode loses nothing)."""
+    finite = [b for b in range(256) if (b & 0x7F) != 0x7F]
+    codes = np.tile(np.arange(256, dtype=np.uint8), (len(finite), 1)).reshape(len(finite), 256)
+    scales = np.repeat(np.array(finite, dtype=np.uint8)[:, None], 32, axis=1)
+    vals = oracle.dequant_fp4(codes, scales)
+    oracle.bf16_bits_exact(vals)                           # raises if any is not exact
