@@ -224,10 +224,20 @@ __device__ __forceinline__ void prefetch_rows(const AttnParams &p, int64_t bidx,
                                               int j1, int lane)
 {
     // lane = 8 * (row within a group of 4) + line
+    const int line = lane & 7;
     for (int j = j0 + (lane >> 3); j < j1; j += 4) {
         const int v = list[j];
-        if (v >= 0 && v < p.N && !(FP4 && v >= p.W))   // fp4 rows: no bf16 row to warm
-            prefetch_l2_line(reinterpret_cast<const uint8_t *>(kv_row<TWO>(p, bidx, v)) + (lane & 7) * 128);
+        if (v < 0 || v >= p.N)
+            continue;
+        if (FP4 && v >= p.W) {   // fp4 row: 256 code bytes and 32 scale bytes
+            const size_t cr = (size_t)bidx * (size_t)p.kv2_bstride + (size_t)(v - p.W);
+            if (line < 2)
+                prefetch_l2_line(p.kv2_codes + cr * (D / 2) + line * 128);
+            else if (line == 2)
+                prefetch_l2_line(p.kv2_scales + cr * (D / 16));
+        } else {
+            prefetch_l2_line(reinterpret_cast<const uint8_t *>(kv_row<TWO>(p, bidx, v)) + line * 128);
+        }
     }
 }
 
@@ -364,39 +374,41 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     __syncwarp();
 }
 
-// OCP FP8 E4M3 (the "fn" variant: bias 7, no infinities, S.1111.111 is NaN).
-__device__ __forceinline__ float e4m3_value(uint32_t b)
+// Two E4M3 ("fn") scale bytes (low byte first) as two bf16 pairs, each
+// holding its scale times 2^112 twice.  The hardware conversion to f16 is
+// exact (E4M3 values are f16 normals), and so are the products and the bf16
+// roundings (at most four significant bits, exponents within range); NaN
+// stays NaN.
+__device__ __forceinline__ void scales_x2112(uint32_t two_bytes, uint32_t &s0, uint32_t &s1)
 {
-    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
-    float v;
-    if (e == 0u)
-        v = (float)m * 0.001953125f;                        // m * 2^-9
-    else if (e == 15u && m == 7u)
-        v = __uint_as_float(0x7fc00000u);                   // NaN
-    else
-        v = __uint_as_float(((e + 120u) << 23) | (m << 20));   // (1 + m/8) * 2^(e-7)
-    return (b & 0x80u) ? -v : v;
+    uint32_t h;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(h) : "r"(two_bytes));
+    const float f0 = __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu))) * 0x1p112f;
+    const float f1 = __half2float(__ushort_as_half((unsigned short)(h >> 16))) * 0x1p112f;
+    s0 = pack_bf16x2(f0, f0);
+    s1 = pack_bf16x2(f1, f1);
 }
 
-// Eight e2m1 codes (nibble k of `codes` = feature k: bit 3 sign, bits 2..0 the
-// magnitude index into 0, 0.5, 1, 1.5, 2, 3, 4, 6) times their group's scale,
-// as four packed bf16 pairs (exact: a code times an E4M3 scale has at most
-// five significant bits).
-__device__ __forceinline__ uint4 dequant_e2m1x8(uint32_t codes, float scale)
+// Eight e2m1 codes (byte i: feature 2i in the low nibble, 2i+1 in the high
+// one) times their group's scale, as four packed bf16 pairs.  The hardware
+// converts each code pair to f16 exactly; a code is zero or an f16 normal
+// whose mantissa has only its top bit, so moving the exponent and mantissa
+// right by three bits gives the bf16 bit pattern of the code times 2^-112,
+// and one bf16 product with `scale2` (scale times 2^112, both halves) gives
+// code times scale, exactly (at most five significant bits).
+__device__ __forceinline__ uint4 dequant_e2m1x8(uint32_t codes, uint32_t scale2)
 {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(codes));
     uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 8; k += 2) {
-        float v[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t c = (codes >> (4 * (k + h))) & 15u, i = c & 7u;
-            // twice the magnitude: 0, 1, 2, 3, 4, 6, 8, 12
-            const uint32_t twice = i < 4u ? i : (2u + (i & 1u)) << ((i >> 1) - 1u);
-            const float mag = (float)twice * 0.5f * scale;
-            v[h] = (c & 8u) ? -mag : mag;
-        }
-        w[k >> 1] = pack_bf16x2(v[0], v[1]);
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t b = ((h[i] >> 3) & 0x0FFF0FFFu) | (h[i] & 0x80008000u);
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(w[i]) : "r"(b), "r"(scale2));
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
@@ -438,13 +450,42 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
         };
         for (int c = 0; c < nc && ok; ++c) {
             const int rows = min(CH, n - c * CH);
-            // this lane's eight (row, 16-byte piece) jobs, rows r0 + 2i; the rows
-            // are the same for both tiles
+            // bf16 rows: this lane's eight (row, 16-byte piece) jobs, rows r0 + 2i;
+            // the rows are the same for both tiles
             const int r0 = ROWS_PER_GATHER_WARP * wg + (lane >> 4);
             int row[8];
+            // fp4 rows: this lane's two rows rf + 8j, 32 features (quarter qq of
+            // the tile: 16 code bytes, 2 scales) of each; the loads of both tiles
+            // are issued before the tiles are free
+            const int qq = lane & 3, rf = ROWS_PER_GATHER_WARP * wg + (lane >> 2);
+            int rv[2];
+            uint4 code[2][2];
+            uint32_t scl[2][2];
+            if constexpr (!FP4) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                row[i] = r0 + 2 * i < rows ? cidx[c * CH + r0 + 2 * i] : -1;
+                for (int i = 0; i < 8; ++i)
+                    row[i] = r0 + 2 * i < rows ? cidx[c * CH + r0 + 2 * i] : -1;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    rv[j] = rf + 8 * j < rows ? cidx[c * CH + rf + 8 * j] : -1;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        code[e][j] = make_uint4(0u, 0u, 0u, 0u);
+                        scl[e][j] = 0u;
+                        if (rv[j] >= p.W) {
+                            const size_t cr = (size_t)bidx * (size_t)p.kv2_bstride + (size_t)(rv[j] - p.W);
+                            const int d = grp + 2 * e;
+                            code[e][j] = __ldg(reinterpret_cast<const uint4 *>(p.kv2_codes + cr * (D / 2) + 64 * d +
+                                                                               16 * qq));
+                            const uint8_t *sp = p.kv2_scales + cr * (D / 16) + 8 * d + 2 * qq;
+                            scl[e][j] = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+                        }
+                    }
+                }
+            }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int d = grp + 2 * e;
@@ -452,8 +493,8 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                 ph_kvfree[e] ^= 1u;
                 if (!ok)
                     break;
-                const int sl = 2 * d + (pc >> 3), ch = pc & 7;
                 if constexpr (!FP4) {
+                    const int sl = 2 * d + (pc >> 3), ch = pc & 7;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int r = r0 + 2 * i;
@@ -462,40 +503,30 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                         cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
                     }
                 } else {
-                    // window rows (and empty slots) by cp.async; compressed rows are
-                    // fp4: eight features = four code bytes and their group's scale,
-                    // loaded for four rows at a time, then decoded into the slot
-                    const int f0 = sl * 64 + ch * 8;
+                    // quarter qq: slice 2d + qq / 2, 16-byte chunks 4 (qq % 2) .. +3
+                    const int sl = 2 * d + (qq >> 1), ch0 = 4 * (qq & 1);
 #pragma unroll
-                    for (int h = 0; h < 8; h += 4) {
-                        uint32_t code[4], scb[4];
+                    for (int j = 0; j < 2; ++j) {
+                        const int r = rf + 8 * j, v = rv[j];
+                        const uint32_t roff = OFF_KV + sl * SLICE_BYTES + r * 128;
+                        if (v >= p.W) {
+                            uint32_t s0, s1;
+                            scales_x2112(scl[e][j], s0, s1);
+                            const uint32_t cw[4] = {code[e][j].x, code[e][j].y, code[e][j].z, code[e][j].w};
 #pragma unroll
-                        for (int i = h; i < h + 4; ++i) {
-                            const int v = row[i];
-                            code[i - h] = 0u;
-                            scb[i - h] = 0u;
-                            if (v >= p.W) {
-                                const size_t cr = (size_t)bidx * (size_t)p.kv2_bstride + (size_t)(v - p.W);
-                                code[i - h] = __ldg(reinterpret_cast<const uint32_t *>(p.kv2_codes + cr * (D / 2) + f0 / 2));
-                                scb[i - h] = __ldg(p.kv2_scales + cr * (D / 16) + f0 / 16);
-                            } else {
-                                const int r = r0 + 2 * i;
-                                const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r * 128 + ((ch ^ (r & 7)) << 4);
-                                // an empty slot copies nothing; its source is any valid row
-                                const uint16_t *src =
-                                    v >= 0 ? kvb + (size_t)v * D + f0
-                                           : (p.W > 0 ? kvb : reinterpret_cast<const uint16_t *>(p.kv2_codes));
-                                cp_async16(dst, src, v < 0 ? 0u : 16u);
-                            }
-                        }
+                            for (int m = 0; m < 4; ++m)
+                                *reinterpret_cast<uint4 *>(smem + roff + (((ch0 + m) ^ (r & 7)) << 4)) =
+                                    dequant_e2m1x8(cw[m], m < 2 ? s0 : s1);
+                        } else {
+                            // window row, or an empty slot (copies nothing; its
+                            // source is any valid address)
+                            const uint16_t *src =
+                                v >= 0 ? kvb + (size_t)v * D + 128 * d + 32 * qq
+                                       : (p.W > 0 ? kvb : reinterpret_cast<const uint16_t *>(p.kv2_codes));
 #pragma unroll
-                        for (int i = h; i < h + 4; ++i) {
-                            if (row[i] >= p.W) {
-                                const int r = r0 + 2 * i;
-                                uint4 *dst = reinterpret_cast<uint4 *>(smem + OFF_KV + sl * SLICE_BYTES + r * 128 +
-                                                                       ((ch ^ (r & 7)) << 4));
-                                *dst = dequant_e2m1x8(code[i - h], e4m3_value(scb[i - h]));
-                            }
+                            for (int m = 0; m < 4; ++m)
+                                cp_async16(sbase + roff + (((ch0 + m) ^ (r & 7)) << 4), v >= 0 ? src + 8 * m : src,
+                                           v < 0 ? 0u : 16u);
                         }
                     }
                 }
@@ -519,7 +550,14 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
             // does not wait for HBM
             if (p.prefetch_rows && c + 1 < nc) {
                 const int j = (c + 1) * CH + ROWS_PER_GATHER_WARP * wg + (lane >> 1);
-                if (j < n && !(FP4 && cidx[j] >= p.W)) {
+                if (j < n && FP4 && cidx[j] >= p.W) {
+                    // fp4 row: group g warms code line g; group 0 also the scales
+                    const size_t cr = (size_t)bidx * (size_t)p.kv2_bstride + (size_t)(cidx[j] - p.W);
+                    if ((lane & 1) == 0)
+                        prefetch_l2_line(p.kv2_codes + cr * (D / 2) + 128 * grp);
+                    else if (grp == 0)
+                        prefetch_l2_line(p.kv2_scales + cr * (D / 16));
+                } else if (j < n) {
                     const uint8_t *rp = reinterpret_cast<const uint8_t *>(row_ptr(cidx[j])) +
                                         (grp + 2 * (lane & 1)) * 256;
                     prefetch_l2_line(rp);

@@ -376,3 +376,30 @@ def test_two_source_fp4_matches_decoded_cache(B, T, K, W, C, host_c):
                                                  512 ** -0.5)
     assert bad == 0
     compare(got.double().cpu().numpy(), ref, f"fp4 two sources B{B} W{W} C{C}")
+
+
+@pytest.mark.gpu
+def test_fp4_every_scale_byte():
+    """Every E4M3 scale byte but the two NaNs (zero, subnormals, up to 448)
+    and every code byte go through the in-kernel decoding: the result equals
+    the bf16 call on the decoded cache bit for bit."""
+    g = torch.Generator().manual_seed(5)
+    B, T, W, C, D = 2, 3, 8, 16, 512
+    win = I.rms_rows(torch.randn(B, W, D, generator=g)).to(torch.bfloat16)
+    codes = torch.randint(0, 256, (B, C, D // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+    codes[0, 0] = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    sb = torch.arange(B * C * (D // 16), dtype=torch.int32) % 256
+    sb[(sb == 0x7F) | (sb == 0xFF)] = 0
+    scales = sb.to(torch.uint8).view(B, C, D // 16)
+    q = (0.01 * torch.randn(B, T, 64, D, generator=g)).to(torch.bfloat16)
+    sink = torch.randn(64, generator=g)
+    idx = torch.arange(W + C, dtype=torch.int32).repeat(B, T, 1)
+    gd = to_dev(dict(q=q, sink=sink, idx=idx))
+    got = sa.sparse_attn_two_source_fp4(gd["q"], win.cuda(), codes.cuda(), scales.cuda(), gd["sink"], gd["idx"],
+                                        512 ** -0.5, W=W, C=C, out_dtype=torch.float32, check=True)
+    decoded = torch.from_numpy(oracle.bf16_bits_exact(
+        oracle.dequant_fp4(codes.numpy(), scales.numpy())).view(np.int16)).view(torch.bfloat16)
+    ref16 = sa.sparse_attn_two_source(gd["q"], win.cuda(), decoded.cuda(), gd["sink"], gd["idx"], 512 ** -0.5,
+                                      W=W, C=C, out_dtype=torch.float32, check=True)
+    assert torch.isfinite(ref16).all()
+    assert torch.equal(got, ref16)
