@@ -38,8 +38,8 @@ HEADLINE = "decode"
 KERNEL_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)),
                           "sparse_latent_attention_02_gb300", "csrc", "sa_attn.cu")
 MEASURED_TRAFFIC = {
-    "decode": ("f14d7d619332aff2905de859c228c655c254f5f0d9e30e1f67c898a48e9ae836", 47_189_504),
-    "prefill": ("f14d7d619332aff2905de859c228c655c254f5f0d9e30e1f67c898a48e9ae836", 1_058_844_672),
+    "decode": ("4ab438e0c373c63c6f1b96810608c4320779ceb8c358e539b76ee989d3a23e16", 47_199_232),
+    "prefill": ("4ab438e0c373c63c6f1b96810608c4320779ceb8c358e539b76ee989d3a23e16", 1_058_521_856),
 }
 
 
