@@ -14,7 +14,10 @@ wrappers:
   -1 as "skip";
 * :func:`inverse_rope`  -- ``apply_rotary_emb(o[..., -rd:], freqs_cis, True)``
   read as consecutive complex pairs rotated by ``-pos * theta**(-2i/rd)``;
-* :func:`wo_a`          -- the block-diagonal ``einsum("bsgd,grd->bsgr")``.
+* :func:`wo_a`          -- the block-diagonal ``einsum("bsgd,grd->bsgr")``;
+* :func:`dequant_fp8_weight` -- the fp8 ``wo_a`` weight (E4M3, fp32 scale per
+  128 x 128 block) dequantized to bf16, as the page's conversion does before
+  the einsum.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against a dense
 masked brute force, closed forms and invariants; nothing here is "parity
@@ -182,6 +185,39 @@ def bf16_bits_exact(x) -> np.ndarray:
     if np.any(u & 0xFFFF):
         raise ValueError("value not representable in bf16")
     return (u >> 16).astype(np.uint16)
+
+
+def round_bf16(x) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns (uint16), rounded to nearest with ties
+    to even (add 0x7FFF plus the kept part's lowest bit, truncate); NaN stays a
+    quiet NaN."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    r = np.where(np.isnan(f), (u >> 16) | 0x40, r)
+    return r.astype(np.uint16)
+
+
+FP8_BLOCK = 128
+
+
+def dequant_fp8_weight(w8, scales) -> np.ndarray:
+    """fp8 grouped ``wo_a`` weight (the "DeepSeek-V4.1 > Output projection"
+    page keeps ``wo_a`` in fp8 and dequantizes it to bf16 before the einsum):
+    E4M3 bytes [rows, cols] with one fp32 scale per 128 x 128 block
+    (scales [ceil(rows/128), ceil(cols/128)]) -> bf16 bit patterns [rows, cols]:
+    the product value x scale rounded to fp32, then to bf16 (both to nearest
+    even).  The fp64 product is exact (4 x 24 significant bits)."""
+    w = np.asarray(w8, dtype=np.uint8)
+    sc = np.asarray(scales, dtype=np.float32).astype(np.float64)
+    rows, cols = w.shape
+    nb_r, nb_c = -(-rows // FP8_BLOCK), -(-cols // FP8_BLOCK)
+    if sc.shape != (nb_r, nb_c):
+        raise ValueError("scales must be [ceil(rows/128), ceil(cols/128)]")
+    s = np.repeat(np.repeat(sc, FP8_BLOCK, axis=0)[:rows], FP8_BLOCK, axis=1)[:, :cols]
+    with np.errstate(invalid="ignore", over="ignore"):
+        prod = (e4m3_values(w) * s).astype(np.float32)
+    return round_bf16(prod)
 
 
 def sparse_attn_two_source_fp4(q, window_kv, W: int, codes, scales, C: int, sink, idx, scale: float,

@@ -460,3 +460,58 @@ def test_fp4_values_are_exact_in_bf16():
     scales = np.repeat(np.array(finite, dtype=np.uint8)[:, None], 32, axis=1)
     vals = oracle.dequant_fp4(codes, scales)
     oracle.bf16_bits_exact(vals)                           # raises if any is not exact
+
+
+def test_e4m3_matches_torch_float8_for_every_byte():
+    """The oracle's E4M3 decoding against PyTorch's float8_e4m3fn dtype, all 256 bytes."""
+    b = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_values(b)
+    lib = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+    ok = ~np.isnan(ours)
+    assert np.array_equal(ours[ok], lib[ok])
+
+
+def test_round_bf16_matches_torch_including_ties():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-130, 120, 200000))).astype(np.float32)
+    special = np.array([0x3F808000, 0x3F818000, 0x3F80FFFF, 0x7F7FFFFF, 0x00000001, 0x80008000,
+                        0x00018000, 0x7F800000, 0xFF800000, 0x80000000], dtype=np.uint32).view(np.float32)
+    x = np.concatenate([x, special])
+    ours = oracle.round_bf16(x)
+    lib = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, lib)
+    # ties to even by hand: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 -> 1
+    assert oracle.round_bf16(np.float32(1 + 2 ** -8)) == 0x3F80
+    assert oracle.round_bf16(np.float32(1 + 3 * 2 ** -8)) == 0x3F82
+
+
+def test_fp8_weight_power_of_two_scales_are_exact():
+    """A power-of-two scale only moves the exponent: the dequantized weight is
+    the E4M3 value times the scale, exactly."""
+    rng = np.random.default_rng(3)
+    w8 = rng.integers(0, 256, (256, 256), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x11
+    sc = np.exp2(rng.integers(-20, 10, (2, 2))).astype(np.float32)
+    got = oracle.dequant_fp8_weight(w8, sc)
+    want = oracle.bf16_bits_exact(oracle.e4m3_values(w8) * np.repeat(np.repeat(sc, 128, 0), 128, 1))
+    assert np.array_equal(got, want)
+
+
+def test_fp8_weight_matches_torch_dequantization_and_block_layout():
+    """General scales: PyTorch's own float8 decoding, fp32 product and bf16
+    rounding agree; each element takes the scale of its own 128 x 128 block
+    (ragged last blocks included), checked element by element."""
+    rng = np.random.default_rng(4)
+    rows, cols = 300, 200
+    w8 = rng.integers(0, 256, (rows, cols), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x22
+    sc = (rng.random((3, 2)) * 1e-2 + 1e-3).astype(np.float32)
+    got = oracle.dequant_fp8_weight(w8, sc)
+    lib_w = torch.from_numpy(w8).view(torch.float8_e4m3fn).float()
+    for i in range(rows):
+        s_row = torch.from_numpy(np.array([sc[i // 128, j // 128] for j in range(cols)], dtype=np.float32))
+        lib = (lib_w[i] * s_row).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got[i], lib), i
+    with pytest.raises(ValueError):
+        oracle.dequant_fp8_weight(w8, sc[:2])
