@@ -455,6 +455,40 @@ def bench_decode_fp4(steps: int, warmup: int, dev, pk: dict) -> dict:
                          "frac": gbs / pk["hbm_gbs"], "peak_note": f"{pk['source']} HBM copy"}}
 
 
+def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict) -> dict:
+    """The fused-tail workload (attention, inverse RoPE, grouped wo_a) with wo_a
+    kept as an fp8 checkpoint (E4M3 + an fp32 scale per 128 x 128 block,
+    dequantized inside the GEMM): same inputs and flops as the bf16 line."""
+    import sparse_latent_attention_02_gb300 as sa
+    wl = I.WORKLOADS["fused_tail"]
+    sets = sets_for(wl, dev)
+    rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).to(dev)
+    fns, wss = [], []
+    for x in sets:
+        x["w8"], x["w8_scales"] = I.fp8_weight(x.pop("wo_a"))
+        y = torch.empty((wl.B, wl.T, wl.G * wl.R), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(sa.fused_workspace_size(wl.B, wl.T, wl.K, wl.G, wl.R), dtype=torch.uint8, device=dev)
+        wss.append(ws)
+        fns.append(lambda x=x, y=y, ws=ws: sa.sparse_attn_rope_wo_a_fp8(
+            x["q"], x["kv"], x["sink"], x["idx"], wl.scale, rope, x["w8"], x["w8_scales"], out=y, workspace=ws))
+    secs, _ = time_graph_steps(fns, steps, warmup)
+    for ws in wss:
+        sa.check_errors(ws)
+    step_s = secs / steps
+    flops = float(np.mean([algorithmic(wl, x["idx"])["flops"] for x in sets]))
+    tflops = flops / step_s / 1e12
+    w_bytes = sets[0]["w8"].numel() + sets[0]["w8_scales"].numel() * 4
+    del sets, fns
+    torch.cuda.empty_cache()
+    return {"workload": f"fused tail with an fp8 wo_a: B={wl.B} T={wl.T} K={wl.K}, wo_a E4M3 "
+                        f"[{wl.G}, {wl.R}, {wl.H * wl.D // wl.G}] + 128x128 block scales ({w_bytes} bytes)",
+            "ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "tflops": tflops,
+            "flops_per_step": int(flops), "gpu_launches": 2 * steps,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops_sustained"],
+                         "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops_sustained"],
+                         "peak_note": f"{pk['source']} sustained bf16 (the products are bf16)"}}
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
     """The fp64 oracle, as it stands, on the host cores: whole decode steps
     (all queries of one input set) repeated until about `budget_s` seconds."""
@@ -519,6 +553,7 @@ def run_ours(args):
             extra[name] = r
         extra["topk"] = bench_topk(max(3, min(args.steps, 50)), max(args.warmup, 3), dev, pk)
         extra["decode_fp4"] = bench_decode_fp4(max(3, min(args.steps, 200)), max(args.warmup, 3), dev, pk)
+        extra["fused_tail_fp8"] = bench_fused_tail_fp8(max(3, min(args.steps, 20)), max(args.warmup, 3), dev, pk)
     sampler.stop()
     e2e = head.pop("e2e", None)
     cpu = (cpu_baseline(args.workload, budget_s=args.cpu_seconds)

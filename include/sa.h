@@ -176,6 +176,31 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
                                    void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * sa_sparse_attn_rope_wo_a with the grouped weight kept in fp8 (the same
+ * page: the checkpoint's wo_a is fp8, its conversion dequantizes it to bf16,
+ * and an fp8 grouped GEMM would halve the weight's memory).  The kernel reads
+ * the E4M3 bytes and dequantizes them in shared memory to exactly the bf16
+ * weight that conversion gives, so the result equals sa_sparse_attn_rope_wo_a
+ * on that bf16 weight:
+ *   W[n, d] = bf16(fp32(e4m3(wo_a_e4m3[n, d]) * wo_a_scales[n / 128, d / 128]))
+ * (n = g*R + r; the product rounded to fp32, then to bf16, both to nearest
+ * even).  The pages do not give the scale layout; one fp32 scale per
+ * 128 x 128 block is taken.
+ *   (q ... rope_dim, G, R, out) as for sa_sparse_attn_rope_wo_a; the same
+ *          workspace size (sa_sparse_attn_rope_wo_a_workspace_size)
+ *   wo_a_e4m3   E4M3 bytes [G, R, H*D/G] contiguous, 16-byte aligned
+ *   wo_a_scales fp32 [G*R/128, H*D/G/128] contiguous, 4-byte aligned
+ * H*D/G must be a multiple of 128 (SA_ERR_UNSUPPORTED otherwise).
+ */
+sa_status sa_sparse_attn_rope_wo_a_fp8(const void *q, const void *kv, const float *sink,
+                                       const int32_t *idx, float scale, int B, int T,
+                                       int H, int D, int N, int K,
+                                       const float *rope_cos_sin, int rope_dim,
+                                       const uint8_t *wo_a_e4m3, const float *wo_a_scales,
+                                       int G, int R, void *out, void *workspace,
+                                       size_t ws_bytes, void *stream);
+
+/*
  * Bytes of workspace `sa_sparse_attn_block_tail` needs: the fused call's
  * workspace plus the bf16 wo_a output [B, T, G*R] kept between the GEMMs.
  */

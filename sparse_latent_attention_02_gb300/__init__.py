@@ -30,7 +30,7 @@ EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_tw
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
            "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail",
-           "sa_topk_indices", "sa_sparse_attn_two_source_fp4")
+           "sa_topk_indices", "sa_sparse_attn_two_source_fp4", "sa_sparse_attn_rope_wo_a_fp8")
 
 
 class SAError(RuntimeError):
@@ -68,6 +68,9 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_sparse_attn_rope_wo_a.restype = I
             lib.sa_sparse_attn_rope_wo_a.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
                                                      V, V, Z, V]
+            lib.sa_sparse_attn_rope_wo_a_fp8.restype = I
+            lib.sa_sparse_attn_rope_wo_a_fp8.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, V, I,
+                                                         I, V, V, Z, V]
             lib.sa_sparse_attn_block_tail_workspace_size.restype = Z
             lib.sa_sparse_attn_block_tail_workspace_size.argtypes = [I, I, I, I, I, I, I]
             lib.sa_sparse_attn_block_tail.restype = I
@@ -345,6 +348,48 @@ def sparse_attn_rope_wo_a(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor,
                                         workspace.numel() * workspace.element_size(),
                                         _stream_ptr(stream))
     _check(code, "sa_sparse_attn_rope_wo_a")
+    if check:
+        check_errors(workspace, stream)
+    return out
+
+
+def sparse_attn_rope_wo_a_fp8(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor,
+                              idx: torch.Tensor, scale: float, rope_cos_sin: torch.Tensor,
+                              wo_a_e4m3: torch.Tensor, wo_a_scales: torch.Tensor,
+                              out: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None, stream=None,
+                              check: bool = False) -> torch.Tensor:
+    """sparse_attn_rope_wo_a with wo_a in fp8: E4M3 bytes uint8 [G, R, H*D/G]
+    and fp32 scales [G*R/128, H*D/G/128], one per 128 x 128 block, dequantized
+    in the kernel to bf16(fp32(value * scale)).  Returns bf16 [B, T, G*R]."""
+    B, T, H, D, N, K = _attn_args(q, kv, sink, idx)
+    _need(rope_cos_sin, "rope_cos_sin", torch.float32, 3)
+    _need(wo_a_e4m3, "wo_a_e4m3", torch.uint8, 3)
+    _need(wo_a_scales, "wo_a_scales", torch.float32, 2)
+    G, R, Din = wo_a_e4m3.shape
+    if rope_cos_sin.shape[0] != T or rope_cos_sin.shape[2] != 2:
+        raise ValueError("rope_cos_sin must be [T, rope_dim/2, 2]")
+    if G * Din != H * D:
+        raise ValueError("wo_a_e4m3 must be [G, R, H*D/G]")
+    if tuple(wo_a_scales.shape) != ((G * R + 127) // 128, (Din + 127) // 128):
+        raise ValueError("wo_a_scales must be [G*R/128, H*D/G/128]")
+    rope_dim = 2 * rope_cos_sin.shape[1]
+    if out is None:
+        out = torch.empty((B, T, G * R), dtype=torch.bfloat16, device=q.device)
+    else:
+        _need(out, "out", torch.bfloat16, 3)
+    lib = library()
+    need = int(lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, H, D, K, G, R))
+    if workspace is None:
+        workspace = _workspace(need, q.device, "fused")
+    code = lib.sa_sparse_attn_rope_wo_a_fp8(q.data_ptr(), kv.data_ptr(), sink.data_ptr(),
+                                            idx.data_ptr(), float(scale), B, T, H, D, N, K,
+                                            rope_cos_sin.data_ptr(), rope_dim, wo_a_e4m3.data_ptr(),
+                                            wo_a_scales.data_ptr(), G, R, out.data_ptr(),
+                                            workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream_ptr(stream))
+    _check(code, "sa_sparse_attn_rope_wo_a_fp8")
     if check:
         check_errors(workspace, stream)
     return out

@@ -145,15 +145,20 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const KvSources &src, c
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // y[m, g*R + r] = sum_d a[m, g*Din + d] * w[g*R + r, d] for m < M (bf16 in and
-// out, fp32 accumulation) on the persistent tcgen05 GEMM.
-sa_status grouped_gemm(const void *a, const void *w, void *y, int64_t M, int G, int R, int Din, void *ws,
-                       int sms, cudaStream_t s)
+// out, fp32 accumulation) on the persistent tcgen05 GEMM.  With w_scales, w
+// is E4M3 bytes with one fp32 scale per 128 x 128 block, dequantized to bf16
+// inside the kernel.
+sa_status grouped_gemm(const void *a, const void *w, const float *w_scales, void *y, int64_t M, int G, int R,
+                       int Din, void *ws, int sms, cudaStream_t s)
 {
     GemmParams g;
     std::memset(&g, 0, sizeof g);
-    if (!encode_tmap_2d(&g.tm_a, a, (uint64_t)M, (uint64_t)G * Din, 64, 128) ||
-        !encode_tmap_2d(&g.tm_b, w, (uint64_t)G * R, (uint64_t)Din, 64, 256))
+    if (!encode_tmap_2d(&g.tm_a, a, (uint64_t)M, (uint64_t)G * Din, 64, 128))
         return SA_ERR_CUDA;
+    if (w_scales ? !encode_tmap_2d_u8(&g.tm_b8, w, (uint64_t)G * R, (uint64_t)Din, 64, 128)
+                 : !encode_tmap_2d(&g.tm_b, w, (uint64_t)G * R, (uint64_t)Din, 64, 256))
+        return SA_ERR_CUDA;
+    g.b_scales = w_scales;
     g.y = static_cast<uint16_t *>(y);
     g.err = static_cast<uint32_t *>(ws);
     g.M = (int)M;
@@ -214,6 +219,21 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows)
+{
+    CUtensorMap probe;
+    if (!encode_tmap_2d(&probe, base, 1, 64, 64, 1))   // resolves the driver entry point once
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace sa
@@ -352,14 +372,19 @@ namespace {
 
 // Host checks of the tail arguments.  rope_dim is a multiple of 32 so that
 // every warp of the epilogue either rotates all of its 32 features or none.
+// fp8 weights (fp8 true): whole 128 x 128 scale blocks and 4-byte aligned scales.
 sa_status check_tail_args(int H, int D, const float *rope_cos_sin, int rope_dim, const void *wo_a, int G,
-                          int R)
+                          int R, bool fp8 = false, const float *wo_a_scales = nullptr)
 {
     if (G <= 0 || R <= 0 || rope_dim < 0)
         return SA_ERR_INVALID_ARG;
     if ((H * D) % G != 0 || ((H * D) / G) % 64 != 0 || R % 256 != 0 || rope_dim % 32 != 0 || rope_dim > D)
         return SA_ERR_UNSUPPORTED;
+    if (fp8 && ((H * D) / G) % 128 != 0)
+        return SA_ERR_UNSUPPORTED;
     if (!wo_a || !aligned(wo_a, 16) || (rope_dim > 0 && !rope_cos_sin))
+        return SA_ERR_INVALID_ARG;
+    if (fp8 && (!wo_a_scales || !aligned(wo_a_scales, 4)))
         return SA_ERR_INVALID_ARG;
     return SA_OK;
 }
@@ -369,8 +394,8 @@ sa_status check_tail_args(int H, int D, const float *rope_cos_sin, int rope_dim,
 // [B*T, G*R] bf16.  Arguments already checked.
 sa_status attn_rope_wo_a(const void *q, const void *kv, const float *sink, const int32_t *idx, float scale,
                          int B, int T, int H, int D, int N, int K, const float *rope_cos_sin, int rope_dim,
-                         const void *wo_a, int G, int R, void *y, void *workspace, size_t attn_ws, int sms,
-                         cudaStream_t s)
+                         const void *wo_a, const float *wo_a_scales, int G, int R, void *y, void *workspace,
+                         size_t attn_ws, int sms, cudaStream_t s)
 {
     const int64_t BT = (int64_t)B * T;
     void *o = static_cast<uint8_t *>(workspace) + attn_ws;
@@ -391,8 +416,8 @@ sa_status attn_rope_wo_a(const void *q, const void *kv, const float *sink, const
         if (launch_attention(p, sch, s) != cudaSuccess)
             return SA_ERR_CUDA;
     }
-    // 2) grouped wo_a
-    return grouped_gemm(o, wo_a, y, BT, G, R, H * D / G, workspace, sms, s);
+    // 2) grouped wo_a (bf16, or fp8 with block scales)
+    return grouped_gemm(o, wo_a, wo_a_scales, y, BT, G, R, H * D / G, workspace, sms, s);
 }
 
 }  // namespace
@@ -421,8 +446,36 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
     const size_t o_bytes = round256((size_t)BT * H * D * 2);
     if (ws_bytes < attn_ws + o_bytes)
         return SA_ERR_WORKSPACE;
-    return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, G, R, out,
-                          workspace, attn_ws, sms, static_cast<cudaStream_t>(stream));
+    return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, nullptr, G, R,
+                          out, workspace, attn_ws, sms, static_cast<cudaStream_t>(stream));
+}
+
+sa_status sa_sparse_attn_rope_wo_a_fp8(const void *q, const void *kv, const float *sink, const int32_t *idx,
+                                       float scale, int B, int T, int H, int D, int N, int K,
+                                       const float *rope_cos_sin, int rope_dim, const uint8_t *wo_a_e4m3,
+                                       const float *wo_a_scales, int G, int R, void *out, void *workspace,
+                                       size_t ws_bytes, void *stream)
+{
+    sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
+    if (st != SA_OK)
+        return st;
+    const int64_t BT = (int64_t)B * T;
+    if (BT == 0)
+        return G <= 0 || R <= 0 || rope_dim < 0 ? SA_ERR_INVALID_ARG : SA_OK;
+    st = check_tail_args(H, D, rope_cos_sin, rope_dim, wo_a_e4m3, G, R, true, wo_a_scales);
+    if (st != SA_OK)
+        return st;
+    if (BT >= ((int64_t)1 << 31) / 128)
+        return SA_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
+    const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
+    const size_t o_bytes = round256((size_t)BT * H * D * 2);
+    if (ws_bytes < attn_ws + o_bytes)
+        return SA_ERR_WORKSPACE;
+    return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a_e4m3,
+                          wo_a_scales, G, R, out, workspace, attn_ws, sms, static_cast<cudaStream_t>(stream));
 }
 
 size_t sa_sparse_attn_block_tail_workspace_size(int B, int T, int H, int D, int K, int G, int R)
@@ -466,12 +519,12 @@ sa_status sa_sparse_attn_block_tail(const void *q, const void *kv, const float *
         return SA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *y = static_cast<uint8_t *>(workspace) + attn_ws + o_bytes;
-    st = attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, G, R, y,
-                        workspace, attn_ws, sms, s);
+    st = attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, nullptr, G, R,
+                        y, workspace, attn_ws, sms, s);
     if (st != SA_OK)
         return st;
     // 3) wo_b: one dense [dim, G*R] projection of the flattened groups
-    return grouped_gemm(y, wo_b, out, BT, 1, dim, G * R, workspace, sms, s);
+    return grouped_gemm(y, wo_b, nullptr, out, BT, 1, dim, G * R, workspace, sms, s);
 }
 
 sa_status sa_topk_indices(const float *scores, int64_t row_stride, int64_t rows, int L, int k, int offset,

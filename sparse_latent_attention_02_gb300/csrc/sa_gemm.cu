@@ -10,7 +10,20 @@
 // K in blocks of 64 features.  Warp 0 feeds a 4-stage shared-memory ring with
 // TMA (128-byte swizzle), warp 1 issues tcgen05.mma (M=128, N=256, K=16) into
 // one of two TMEM accumulators, warps 2-5 drain the other accumulator to bf16.
+//
+// fp8 weights (the page notes that an fp8 grouped GEMM would halve the
+// weight's memory): W is stored as E4M3 with one fp32 scale per 128 x 128
+// block.  Tiles are 256 tokens x 128 rank columns (two M=128 MMAs share each
+// weight block, so every weight is decoded once per 256 tokens), in the same
+// four 48 KB stages.  Warp 14 streams the 128 x 64 blocks of raw E4M3 bytes
+// by TMA into a ring of their own, ahead of the stages; warps 6-13 write each
+// into its stage's swizzled bf16 weight slot as bf16(fp32(value * scale)) --
+// the weight the page's bf16 conversion would give -- as soon as the MMAs
+// have released the slot, while the activations' TMA for the same stage is
+// in flight.  Only the weight's bytes change; the products are the bf16
+// GEMM's.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
@@ -18,20 +31,71 @@
 namespace sa {
 namespace gemm {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int THREADS = 192;
-constexpr uint32_t A_BYTES = BM * BK * 2;     // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;     // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
-constexpr uint32_t OFF_MISC = OFF_BAR + 16 * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+constexpr int BK = 64;
+constexpr int FP8_BLOCK = 128;                // weight rows / columns per fp32 scale
+constexpr int CONV_WARP0 = 6, CONV_THREADS = 256;
+constexpr int RAW_WARP = CONV_WARP0 + CONV_THREADS / 32;   // 14: TMA of the raw weights
 
-enum : uint32_t { B_FULL0 = 0, B_EMPTY0 = STAGES, B_ACCFULL0 = 2 * STAGES, B_ACCEMPTY0 = 2 * STAGES + 2,
-                  B_DONE = 2 * STAGES + 4, NUM_BARS };
-static_assert(NUM_BARS <= 16, "barrier area");
-constexpr uint32_t IDESC = idesc_bf16(BM, BN, 0, 0);
+template <bool FP8>
+struct Cfg {
+    static constexpr int BM = FP8 ? 256 : 128;                 // tokens per tile
+    static constexpr int BN = FP8 ? 128 : 256;                 // rank columns per tile
+    static constexpr int HALVES = BM / 128;                    // M=128 MMAs per K step
+    static constexpr uint32_t A_BYTES = BM * BK * 2;           // 16 / 32 KB
+    static constexpr uint32_t B_BYTES = BN * BK * 2;           // 32 / 16 KB
+    static constexpr uint32_t RAW_BYTES = FP8 ? BN * BK : 0;   // raw E4M3 weights of one K block
+    static constexpr uint32_t ACC_COLS = HALVES * BN;          // TMEM columns of one accumulator
+    static constexpr int STAGES = 4;
+    static constexpr int THREADS = FP8 ? 192 + CONV_THREADS + 32 : 192;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t OFF_RAW = STAGES * STAGE_BYTES;  // raw ring, one slot per stage
+    static constexpr uint32_t OFF_BAR = OFF_RAW + STAGES * RAW_BYTES;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+    static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
+    // barriers: TMA full, stage empty, converted (fp8), raw full / free (fp8),
+    // accumulators, done
+    static constexpr uint32_t B_FULL0 = 0, B_EMPTY0 = STAGES, B_CONV0 = 2 * STAGES, B_RAWFULL0 = 3 * STAGES,
+                              B_RAWFREE0 = 4 * STAGES, B_ACCFULL0 = 5 * STAGES, B_ACCEMPTY0 = B_ACCFULL0 + 2,
+                              B_DONE = B_ACCEMPTY0 + 2, NUM_BARS = B_DONE + 1;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(NUM_BARS <= 32, "barrier area");
+    static_assert(2 * ACC_COLS <= 512, "two accumulators in TMEM");
+    static_assert(!FP8 || BN % FP8_BLOCK == 0, "a weight tile spans whole scale blocks");
+};
+
+// Sixteen E4M3 weights times their block's scale, as sixteen bf16 (two
+// 16-byte pieces): each byte pair is converted to f16 by the hardware
+// (exact), widened to fp32 (exact), multiplied by the scale with one fp32
+// rounding and rounded to bf16.
+__device__ __forceinline__ void dequant_e4m3x16(const uint4 &w, float scale, uint4 &lo, uint4 &hi)
+{
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h0, h1;
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+            : "=r"(h0), "=r"(h1)
+            : "r"(in[i]));
+        const __half2 p0 = *reinterpret_cast<const __half2 *>(&h0), p1 = *reinterpret_cast<const __half2 *>(&h1);
+        out[2 * i] = pack_bf16x2(__fmul_rn(__low2float(p0), scale), __fmul_rn(__high2float(p0), scale));
+        out[2 * i + 1] = pack_bf16x2(__fmul_rn(__low2float(p1), scale), __fmul_rn(__high2float(p1), scale));
+    }
+    lo = make_uint4(out[0], out[1], out[2], out[3]);
+    hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+// Warp-uniform bounded wait (lane 0 polls).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          uint64_t limit_ns, int lane)
+{
+    int ok = 0;
+    if (lane == 0)
+        ok = bounded_wait(bar, parity, abort_flag, limit_ns) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
 
 struct TileMap {
     int num_m, num_n, total;
@@ -44,8 +108,16 @@ struct TileMap {
     }
 };
 
-__global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant__ GemmParams p)
+template <bool FP8>
+__global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid_constant__ GemmParams p)
 {
+    using C = Cfg<FP8>;
+    constexpr int STAGES = C::STAGES, BM = C::BM, BN = C::BN;
+    constexpr uint32_t STAGE_BYTES = C::STAGE_BYTES, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
+    constexpr uint32_t A_BYTES = C::A_BYTES;
+    constexpr uint32_t B_FULL0 = C::B_FULL0, B_EMPTY0 = C::B_EMPTY0, B_CONV0 = C::B_CONV0,
+                       B_RAWFULL0 = C::B_RAWFULL0, B_RAWFREE0 = C::B_RAWFREE0, B_ACCFULL0 = C::B_ACCFULL0,
+                       B_ACCEMPTY0 = C::B_ACCEMPTY0, B_DONE = C::B_DONE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -65,6 +137,9 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar0 + 8 * (B_FULL0 + s), 1);
             mbar_init(bar0 + 8 * (B_EMPTY0 + s), 1);
+            mbar_init(bar0 + 8 * (B_CONV0 + s), CONV_THREADS / 32);
+            mbar_init(bar0 + 8 * (B_RAWFULL0 + s), 1);
+            mbar_init(bar0 + 8 * (B_RAWFREE0 + s), CONV_THREADS / 32);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar0 + 8 * (B_ACCFULL0 + a), 1);
@@ -74,7 +149,7 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tm_a);
-        prefetch_tmap(&p.tm_b);
+        prefetch_tmap(FP8 ? &p.tm_b8 : &p.tm_b);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -101,9 +176,13 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
                     }
                     const uint32_t fb = bar0 + 8 * (B_FULL0 + stage);
                     const uint32_t sa_ = sbase + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    tma_load_2d(sa_, &p.tm_a, g * p.Din + kb * BK, mb * BM, fb);
-                    tma_load_2d(sa_ + A_BYTES, &p.tm_b, kb * BK, g * p.R + nb * BN, fb);
+                    mbar_arrive_expect_tx(fb, A_BYTES + (FP8 ? 0u : C::B_BYTES));
+                    // activations: 128-row boxes (rows past M read as zero)
+#pragma unroll
+                    for (int h = 0; h < C::HALVES; ++h)
+                        tma_load_2d(sa_ + h * 128 * BK * 2, &p.tm_a, g * p.Din + kb * BK, mb * BM + 128 * h, fb);
+                    if (!FP8)
+                        tma_load_2d(sa_ + A_BYTES, &p.tm_b, kb * BK, g * p.R + nb * BN, fb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -137,9 +216,11 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
                 }
                 acc_ph[a] ^= 1u;
                 tc_fence_after();
-                const uint32_t dt = tmem + (uint32_t)(a * BN);
+                const uint32_t dt = tmem + (uint32_t)(a * C::ACC_COLS);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!bounded_wait(bar0 + 8 * (B_FULL0 + stage), ph, abort_flag, p.timeout_ns)) {
+                    // the stage's TMA has landed; fp8: the converters are done too
+                    if (!bounded_wait(bar0 + 8 * (B_FULL0 + stage), ph, abort_flag, p.timeout_ns) ||
+                        (FP8 && !bounded_wait(bar0 + 8 * (B_CONV0 + stage), ph, abort_flag, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
@@ -147,9 +228,12 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
                     const uint32_t sa_ = sbase + stage * STAGE_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = smem_desc_sw128(sa_ + k * 32, 16, 1024);
                         const uint64_t bd = smem_desc_sw128(sa_ + A_BYTES + k * 32, 16, 1024);
-                        mma_bf16_ss(dt, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < C::HALVES; ++h) {
+                            const uint64_t ad = smem_desc_sw128(sa_ + h * 128 * BK * 2 + k * 32, 16, 1024);
+                            mma_bf16_ss(dt + (uint32_t)(h * BN), ad, bd, C::IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit(bar0 + 8 * (B_EMPTY0 + stage));
                     if (++stage == STAGES) {
@@ -167,10 +251,94 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
                     break;
         }
         __syncwarp();
+    } else if (FP8 && warp == RAW_WARP) {
+        // ---------------- TMA of the raw E4M3 weight blocks into their ring
+        if (lane == 0) {
+            uint32_t slot = 0, ph = 0, issued = 0;
+            bool ok = true;
+            for (int id = blockIdx.x; id < tm.total && ok; id += gridDim.x) {
+                int g, mb, nb;
+                tm.at(id, g, mb, nb);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!bounded_wait(bar0 + 8 * (B_RAWFREE0 + slot), ph ^ 1u, abort_flag, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar0 + 8 * (B_RAWFULL0 + slot);
+                    mbar_arrive_expect_tx(fb, C::RAW_BYTES);
+                    tma_load_2d(sbase + C::OFF_RAW + slot * C::RAW_BYTES, &p.tm_b8, kb * BK, g * p.R + nb * BN, fb);
+                    ++issued;
+                    if (++slot == STAGES) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            for (uint32_t k = 0; k < STAGES && k < issued; ++k) {
+                const uint32_t n = issued - 1 - k;
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(bar0 + 8 * (B_RAWFULL0 + n % STAGES), (n / STAGES) & 1u))
+                    if (globaltimer_ns() - t0 > p.timeout_ns)
+                        break;
+            }
+        }
+        __syncwarp();
+    } else if (FP8 && warp >= CONV_WARP0) {
+        // ---------------- fp8 weights -> swizzled bf16 operand (warps 6..13).
+        // Thread ct converts 16-byte pieces i = ct + 256 it of the raw BN x 64
+        // block (row i / 4, piece i % 4 = features 16 (i % 4) ..); the block lies
+        // in one 128 x 128 scale block.  Raw slot and stage advance together.
+        const int ct = threadIdx.x - CONV_WARP0 * 32;
+        const int scale_cols = p.Din / FP8_BLOCK;
+        constexpr int ITEMS = BN * BK / 16 / CONV_THREADS;
+        static_assert(ITEMS * CONV_THREADS * 16 == BN * BK, "converter items");
+        uint32_t stage = 0, ph = 0;
+        bool ok = true;
+        for (int id = blockIdx.x; id < tm.total && ok; id += gridDim.x) {
+            int g, mb, nb;
+            tm.at(id, g, mb, nb);
+            const int n0 = g * p.R + nb * BN;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                // the raw block has landed and the MMAs have released the stage
+                ok = warp_wait(bar0 + 8 * (B_RAWFULL0 + stage), ph, abort_flag, p.timeout_ns, lane) &&
+                     warp_wait(bar0 + 8 * (B_EMPTY0 + stage), ph ^ 1u, abort_flag, p.timeout_ns, lane);
+                if (!ok)
+                    break;
+                const float s = __ldg(p.b_scales + (size_t)(n0 / FP8_BLOCK) * scale_cols + (kb * BK) / FP8_BLOCK);
+                const uint8_t *raw = smem + C::OFF_RAW + stage * C::RAW_BYTES;
+                uint8_t *dst = smem + stage * STAGE_BYTES + A_BYTES;
+                uint4 w[ITEMS];
+#pragma unroll
+                for (int it = 0; it < ITEMS; ++it) {
+                    const int i = ct + CONV_THREADS * it;
+                    w[it] = *reinterpret_cast<const uint4 *>(raw + (i >> 2) * BK + 16 * (i & 3));
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar0 + 8 * (B_RAWFREE0 + stage));
+#pragma unroll
+                for (int it = 0; it < ITEMS; ++it) {
+                    const int i = ct + CONV_THREADS * it, r = i >> 2, j = i & 3;
+                    uint4 lo, hi;
+                    dequant_e4m3x16(w[it], s, lo, hi);
+                    *reinterpret_cast<uint4 *>(dst + r * 128 + (((2 * j) ^ (r & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(dst + r * 128 + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar0 + 8 * (B_CONV0 + stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
     } else {
-        // ---------------- epilogue: warps 2..5 -> TMEM lane quarters 2,3,0,1
+        // ---------------- epilogue: warps 2..5 -> TMEM lane quarters 2,3,0,1;
+        // accumulator half h holds tile rows 128h .. 128h+127
         const int quarter = warp & 3;
-        const int row_in_tile = quarter * 32 + lane;
+        const int row_in_half = quarter * 32 + lane;
         uint32_t acc_ph[2] = {0, 0};
         int local = 0;
         for (int id = blockIdx.x; id < tm.total; id += gridDim.x, ++local) {
@@ -185,23 +353,26 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
             tc_fence_after();
             int g, mb, nb;
             tm.at(id, g, mb, nb);
-            const int m = mb * BM + row_in_tile;
-            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * BN);
-            uint16_t *yrow = p.y + (size_t)m * (p.G * p.R) + g * p.R + nb * BN;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(ta + 32 * c, v);
-                tmem_wait_ld();
-                if (m < p.M) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * c);
+            for (int h = 0; h < C::HALVES; ++h) {
+                const int m = mb * BM + 128 * h + row_in_half;
+                const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * C::ACC_COLS + h * BN);
+                uint16_t *yrow = p.y + (size_t)m * (p.G * p.R) + g * p.R + nb * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(ta + 32 * c, v);
+                    tmem_wait_ld();
+                    if (m < p.M) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * c);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[j] = make_uint4(
-                            pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
-                            pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                            pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                            pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                    }
                 }
             }
             tc_fence_before();
@@ -223,15 +394,20 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_kernel(const __grid_constant_
 
 cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st)
 {
-    cudaError_t e = cudaFuncSetAttribute(gemm::wo_a_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)gemm::SMEM_BYTES);
+    const bool fp8 = p.b_scales != nullptr;
+    void (*kernel)(GemmParams) = fp8 ? gemm::wo_a_kernel<true> : gemm::wo_a_kernel<false>;
+    const int smem = (int)(fp8 ? gemm::Cfg<true>::SMEM_BYTES : gemm::Cfg<false>::SMEM_BYTES);
+    const int threads = fp8 ? gemm::Cfg<true>::THREADS : gemm::Cfg<false>::THREADS;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess)
         return e;
-    const int tiles = ((p.M + gemm::BM - 1) / gemm::BM) * (p.R / gemm::BN) * p.G;
+    const int bm = fp8 ? gemm::Cfg<true>::BM : gemm::Cfg<false>::BM;
+    const int bn = fp8 ? gemm::Cfg<true>::BN : gemm::Cfg<false>::BN;
+    const int tiles = ((p.M + bm - 1) / bm) * (p.R / bn) * p.G;
     const int grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0)
         return cudaSuccess;
-    gemm::wo_a_kernel<<<grid, gemm::THREADS, gemm::SMEM_BYTES, st>>>(p);
+    kernel<<<grid, threads, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -65,6 +65,8 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st);
 struct GemmParams {
     CUtensorMap tm_a;          // o as 2-D [M rows, G*Din cols] bf16, box 64x128
     CUtensorMap tm_b;          // W as 2-D [G*R rows, Din cols] bf16, box 64x256
+    CUtensorMap tm_b8;         // fp8 W: E4M3 bytes [G*R rows, Din cols], box 64x128, no swizzle
+    const float *b_scales;     // fp8 W: fp32 [G*R/128, Din/128] block scales; null for bf16 W
     uint16_t *y;               // bf16 [M, G*R]
     uint32_t *err;
     int M, G, R, Din;
@@ -85,5 +87,8 @@ sa_status check_attn_args(const void *q, const void *kv, const float *sink, cons
 // Encode a 2-D bf16 tensor map (row-major [rows, cols], 128B swizzle).
 bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint32_t box_cols, uint32_t box_rows);
+// Encode a 2-D byte tensor map (row-major [rows, cols], no swizzle).
+bool encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                       uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace sa

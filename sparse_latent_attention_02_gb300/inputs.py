@@ -213,3 +213,22 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu") -> dict:
         out["wo_b"] = (0.02 * torch.randn((wl.dim, wl.G * wl.R), generator=gb, device=device,
                                           dtype=torch.float32)).to(torch.bfloat16)
     return out
+
+
+def fp8_weight(w: torch.Tensor, block: int = 128) -> tuple[torch.Tensor, torch.Tensor]:
+    """A synthetic fp8 checkpoint of a weight [rows, cols] (or [G, R, cols],
+    rows = G*R): one fp32 scale per block x block tile, the tile's largest
+    magnitude over 448 (the largest E4M3 value), and the E4M3 bytes of
+    weight / scale (PyTorch's float8_e4m3fn conversion).  Returns
+    (uint8 bytes shaped like w, fp32 scales [ceil(rows/block), ceil(cols/block)])."""
+    shape = w.shape
+    w2 = w.reshape(-1, shape[-1]).float()
+    rows, cols = w2.shape
+    nb_r, nb_c = -(-rows // block), -(-cols // block)
+    pad = torch.zeros(nb_r * block, nb_c * block, dtype=torch.float32, device=w.device)
+    pad[:rows, :cols] = w2.abs()
+    amax = pad.view(nb_r, block, nb_c, block).amax(dim=(1, 3))
+    scales = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    s_full = scales.repeat_interleave(block, 0)[:rows].repeat_interleave(block, 1)[:, :cols]
+    codes = (w2 / s_full).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.reshape(shape).contiguous(), scales.contiguous()

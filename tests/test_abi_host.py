@@ -160,3 +160,23 @@ def test_binding_rejects_cpu_tensors():
         sa.sparse_attn(q, kv, torch.zeros(64), torch.zeros(1, 1, 4, dtype=torch.int32), 0.1)
     with pytest.raises(TypeError):
         sa.sparse_attn(q.float(), kv, torch.zeros(64), torch.zeros(1, 1, 4, dtype=torch.int32), 0.1)
+
+
+def test_fused_fp8_argument_checks(lib):
+    def call(**kw):
+        a = dict(q=16, kv=16, sink=16, idx=16, scale=0.1, B=1, T=1, H=64, D=512, N=8, K=4,
+                 rope=16, rope_dim=64, w8=16, sc=16, G=8, R=1024, out=16, ws=256, wsb=1 << 30,
+                 stream=None)
+        a.update(kw)
+        return lib.sa_sparse_attn_rope_wo_a_fp8(a["q"], a["kv"], a["sink"], a["idx"], a["scale"],
+                                                a["B"], a["T"], a["H"], a["D"], a["N"], a["K"],
+                                                a["rope"], a["rope_dim"], a["w8"], a["sc"], a["G"],
+                                                a["R"], a["out"], a["ws"], a["wsb"], a["stream"])
+    assert call(sc=None) == INVALID               # fp8 weights need their scales
+    assert call(sc=18) == INVALID                 # scales 4-byte aligned
+    assert call(w8=None) == INVALID
+    assert call(w8=8) == INVALID                  # weights 16-byte aligned
+    assert call(G=512) == UNSUPPORTED             # 64 features per group: not whole 128-wide scale blocks
+    assert call(R=1000) == UNSUPPORTED
+    assert call(G=0) == INVALID
+    assert call(B=0, q=None, out=None) == OK      # empty problems touch nothing

@@ -403,3 +403,89 @@ def test_fp4_every_scale_byte():
                                       W=W, C=C, out_dtype=torch.float32, check=True)
     assert torch.isfinite(ref16).all()
     assert torch.equal(got, ref16)
+
+
+@pytest.mark.parametrize("B,T,K,N,G,R", [
+    (2, 300, 192, 400, 8, 512),     # 600 tokens: four full 128-token tiles and a ragged one
+    (1, 130, 640, 1000, 4, 256),    # wider groups (8192 features per group)
+    (3, 7, 64, 100, 16, 256),       # narrow groups (2048 features), one partial tile
+])
+def test_fused_tail_fp8_matches_dequantized_weight(B, T, K, N, G, R):
+    """wo_a kept in fp8 (E4M3 + a scale per 128 x 128 block): the result equals
+    the bf16 fused call on the weight the oracle dequantizes, bit for bit, and
+    the oracle chain on sampled rows."""
+    g = torch.Generator().manual_seed(B * 100 + G)
+    q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16)
+    kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16)
+    sink = torch.randn(64, generator=g)
+    idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
+    idx[torch.rand(B, T, K, generator=g) < 0.1] = -1
+    w = 0.02 * torch.randn(G, R, 64 * 512 // G, generator=g)
+    w8, sc = I.fp8_weight(w)
+    wdq = torch.from_numpy(oracle.dequant_fp8_weight(w8.reshape(G * R, -1).numpy(), sc.numpy())
+                           .view(np.int16)).view(torch.bfloat16).reshape(G, R, -1)
+    rope = sa.rope_table(160000.0, 0, T, 64).cuda()
+    x = to_dev(dict(q=q, kv=kv, sink=sink, idx=idx))
+    got = sa.sparse_attn_rope_wo_a_fp8(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5, rope, w8.cuda(),
+                                       sc.cuda(), check=True)
+    ref16 = sa.sparse_attn_rope_wo_a(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5, rope, wdq.cuda(),
+                                     check=True)
+    assert torch.equal(got, ref16)
+    qs = sample_queries(B * T, 12, seed=G, include=(0, B * T - 1))
+    o = oracle_rows(dict(q=q, kv=kv, sink=sink, idx=idx), qs, 512 ** -0.5)
+    o = oracle.inverse_rope(o, qs % T, 64, 160000.0)
+    yref = oracle.wo_a(o.reshape(len(qs), G, -1), wdq)
+    compare(got.reshape(-1, G * R)[torch.as_tensor(qs, device="cuda")].double().cpu().numpy(),
+            yref.reshape(len(qs), -1), f"fp8 tail G{G}")
+
+
+def test_fused_tail_fp8_workload_sampled():
+    """The fused-tail workload (B=2, T=4096) with its wo_a as an fp8 checkpoint."""
+    wl = I.WORKLOADS["fused_tail"]
+    x = I.make_inputs(wl, seed=4, device="cuda")
+    w8, sc = I.fp8_weight(x["wo_a"])
+    rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).cuda()
+    y = sa.sparse_attn_rope_wo_a_fp8(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, rope, w8, sc, check=True)
+    wdq = torch.from_numpy(oracle.dequant_fp8_weight(w8.reshape(wl.G * wl.R, -1).cpu().numpy(),
+                                                     sc.cpu().numpy()).view(np.int16)).view(torch.bfloat16)
+    qs = sample_queries(wl.n_queries, 16, seed=6, include=(0, 4095, 4096, 8191))
+    o = oracle_rows(x, qs, wl.scale)
+    o = oracle.inverse_rope(o, qs % wl.T, wl.rope_dim, wl.theta)
+    yref = oracle.wo_a(o.reshape(len(qs), wl.G, -1), wdq.reshape(wl.G, wl.R, -1))
+    got = y.reshape(-1, wl.G * wl.R)[torch.as_tensor(qs, device="cuda")].double().cpu().numpy()
+    compare(got, yref.reshape(len(qs), -1), "fused_tail fp8")
+
+
+def test_fused_tail_fp8_special_weights():
+    """fp8 weights with NaN bytes, zero and subnormal-scale blocks, and scales
+    of 256 and more (decoded by the conversion-unit path): the bf16 call on the
+    oracle's dequantized weight gives the same outputs, NaN in the same
+    places."""
+    g = torch.Generator().manual_seed(77)
+    B, T, K, N, G, R = 1, 40, 64, 80, 8, 256
+    din = 64 * 512 // G
+    q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16)
+    kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16)
+    sink = torch.randn(64, generator=g)
+    idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
+    w8 = torch.randint(0, 256, (G, R, din), generator=g, dtype=torch.int32).to(torch.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x33
+    w8[1, 5, 17] = 0x7F                     # two NaN weights: rows 1*256+5 and 3*256+200 become NaN
+    w8[3, 200, 1000] = 0xFF
+    sc = (torch.rand(G * R // 128, din // 128, generator=g) * 1e-3 + 1e-5)
+    sc[0, 0] = 300.0                        # conversion-unit path
+    sc[2, 3] = 2.0 ** 20
+    sc[4, 1] = 1e-40                        # subnormal scale
+    sc[5, 2] = 0.0                          # zero block
+    wdq = torch.from_numpy(oracle.dequant_fp8_weight(w8.reshape(G * R, -1).numpy(), sc.numpy())
+                           .view(np.int16)).view(torch.bfloat16).reshape(G, R, -1)
+    rope = sa.rope_table(160000.0, 0, T, 64).cuda()
+    x = to_dev(dict(q=q, kv=kv, sink=sink, idx=idx))
+    got = sa.sparse_attn_rope_wo_a_fp8(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5, rope, w8.cuda(),
+                                       sc.cuda(), check=True).float()
+    ref = sa.sparse_attn_rope_wo_a(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5, rope, wdq.cuda(),
+                                   check=True).float()
+    nan = torch.isnan(ref)
+    assert torch.equal(torch.isnan(got), nan)
+    assert nan[..., 1 * R + 5].all() and nan[..., 3 * R + 200].all() and nan.sum() == 2 * B * T
+    assert torch.equal(got[~nan], ref[~nan])
