@@ -37,6 +37,7 @@
 //     all roles leave their loops, in-flight copies and MMAs are drained, TMEM
 //     is released and the error word gets ERRBIT_TIMEOUT.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
@@ -692,12 +693,25 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 // then applies the inverse RoPE when asked and writes its heads.  Softmax
 // warps only: warp (quarter qd, half hf) handles features 128d + 32qd + lane
 // of tiles d = 2hf, 2hf + 1.  False when a wait ran out.
+// 2^-e for a row sum l = f * 2^e, f in [0.5, 1) (0 for l = 0): scaling a
+// piece's O by it is exact and leaves every entry within the largest |value|
+// of the rows it sums (|O| <= l * max|v| and 2^-e <= 1 / l).
+__device__ __forceinline__ float row_scale(float l)
+{
+    int e;
+    (void)frexpf(l, &e);
+    return l > 0.f ? ldexpf(1.f, -e) : 0.f;
+}
+
 template <int P>
 __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl, const Seg &s,
                               int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
 {
     constexpr int HP = H / P;
-    constexpr uint32_t SLOT_BYTES = HP * D * 4;      // one piece's O for HP heads, [HP][512] fp32
+    // one piece's O for HP heads, [HP][512], sent as fp16 after an exact
+    // power-of-two scaling by row_scale(l) (bounded then by the largest |value|
+    // of the rows; integers and their halvings stay exact)
+    constexpr uint32_t SLOT_BYTES = HP * D * 2;
     constexpr uint32_t STAT_BYTES = 2 * HP * 4;      // its (m, l) for HP heads
     constexpr int COPY_PARTS = 8;                    // a slot goes as 8 copies issued by 8 threads
     const uint32_t me = cluster_ctarank();
@@ -706,8 +720,10 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     const float *lt = reinterpret_cast<const float *>(smem + OFF_AUX);   // this piece's row sums
     const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);
     float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights, then [HP] 1/den
-    const float *recv = reinterpret_cast<const float *>(smem + OFF_KV);   // [P][HP][512] fp32
-    float *stage = reinterpret_cast<float *>(smem + OFF_KV + me * SLOT_BYTES);
+    float *inv_l = wts;                                       // [64] row_scale(l) while sending
+    // [P][HP / 2][512] pairs of heads (2j, 2j + 1) per feature
+    const __half2 *recv = reinterpret_cast<const __half2 *>(smem + OFF_KV);
+    __half2 *stage = reinterpret_cast<__half2 *>(smem + OFF_KV + me * SLOT_BYTES);
     float *xsend = reinterpret_cast<float *>(smem + OFF_XSEND);
     const int fl = 32 * qd + lane;   // feature within a 128-feature tile
 
@@ -715,6 +731,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         mbar_arrive_expect_tx(bar0 + 8 * B_XFULL, (P - 1) * (SLOT_BYTES + STAT_BYTES));
     if (t < P && t != (int)me)
         mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
+    if (t < H)
+        inv_l[t] = row_scale(lt[t]);
     bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
     if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
         return false;
@@ -750,8 +768,10 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                     v[i] = 0u;
             }
 #pragma unroll
-            for (int i = 0; i < HP; ++i)
-                stage[i * D + 128 * d + fl] = __uint_as_float(v[i]);
+            for (int i = 0; i < HP; i += 2)
+                stage[(i / 2) * D + 128 * d + fl] =
+                    __floats2half2_rn(__uint_as_float(v[i]) * inv_l[g * HP + i],
+                                      __uint_as_float(v[i + 1]) * inv_l[g * HP + i + 1]);
         }
         fence_proxy_async_smem();
         bar_sync(1, SMX_THREADS);
@@ -786,7 +806,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             const float mr = r == (int)me ? m_s[h] : xst[r * 2 * HP + t];
             const float lr = r == (int)me ? lt[h] : xst[r * 2 * HP + HP + t];
             const float w = M == -INFINITY ? 0.f : ex2(mr - M);
-            wts[r * HP + t] = w;
+            // peers' O arrive multiplied by row_scale(l): undo it exactly
+            wts[r * HP + t] = r == (int)me ? w : (lr > 0.f ? w / row_scale(lr) : 0.f);
             den += w * lr;
         }
         den += M == -INFINITY ? 0.f : ex2(sl - M);
@@ -820,8 +841,11 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             if (r == (int)me)
                 continue;
 #pragma unroll
-            for (int i = 0; i < HP; ++i)
-                o[i] += wts[r * HP + i] * recv[(r * HP + i) * 512 + f];
+            for (int i = 0; i < HP; i += 2) {
+                const float2 x = __half22float2(recv[(r * HP + i) / 2 * 512 + f]);
+                o[i] += wts[r * HP + i] * x.x;
+                o[i + 1] += wts[r * HP + i + 1] * x.y;
+            }
         }
 #pragma unroll
         for (int i = 0; i < HP; ++i)
