@@ -325,8 +325,8 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
     Seg s, sn;
     bool have = seg_next(p, it, s);
     if (have) {
-        stage_list(p, s, raw_u32, lane);
-        // the first segment's Q is requested before its list is read
+        // the kernel's prologue already started copying the first list;
+        // the first segment's Q is requested before that list is read
         ok = load_q(p, sbase, s, ph_qempty, q_loads, abort_flag, lane);
     }
     for (int k = 0; ok && have; ++k) {
@@ -337,6 +337,11 @@ __device__ void control_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
         if (!ok)
             break;
         cp_async_wait_all();
+        if (k == 0) {   // the sinks arrived with the first list: to log2 units
+            float *sink_s = reinterpret_cast<float *>(smem + OFF_SINK);
+            sink_s[lane] *= LOG2E;
+            sink_s[lane + 32] *= LOG2E;
+        }
         __syncwarp();
         int32_t *cidx = reinterpret_cast<int32_t *>(smem + OFF_IDX) + b * SA_MAX_K;
         bool bad = false;
@@ -1160,8 +1165,20 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);
     }
-    if (threadIdx.x < 64)
-        reinterpret_cast<float *>(smem + OFF_SINK)[threadIdx.x] = __ldg(p.sink + threadIdx.x) * LOG2E;
+    // the control warp starts copying the sinks and the first index list now,
+    // so that their latency overlaps the rest of the set-up; it waits for the
+    // copies, scales the sinks and publishes both with the first list
+    if (warp == WARP_CONTROL) {
+        cp_async4(sbase + OFF_SINK + 4u * lane, p.sink + lane);
+        cp_async4(sbase + OFF_SINK + 4u * (lane + 32), p.sink + lane + 32);
+        SegIter it;
+        seg_begin(p, it);
+        Seg s;
+        if (seg_next(p, it, s))
+            stage_list(p, s, sbase + OFF_RAW, lane);
+        else
+            cp_async_commit();
+    }
     if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
         tmem_relinquish();
