@@ -11,23 +11,31 @@
 //
 // One CTA per row.  Scores become order-preserving 32-bit keys; a four-pass
 // radix select (8 bits per pass, most significant first) finds the k-th
-// largest key; one ordered pass then writes every position above it and the
-// first positions equal to it, with block-wide prefix counts so that the
-// output is in ascending position order.  Rows of up to CACHE_KEYS scores
-// keep their keys in shared memory; longer rows are read again from global
-// memory (L2) on every pass.
+// largest key: each pass histograms the keys that share the prefix chosen so
+// far (in the first pass, where a few bins take most keys, lanes of a warp
+// that hit the same bin add together) and a block-wide scan over the bins, largest
+// first, picks the bin that holds the k-th key.  The first pass is folded
+// into the pass that computes the keys.  The ordered pass gives each warp a
+// contiguous range of positions: the warps count their keys above the
+// threshold and equal to it, and then write, with ballots, every position
+// above it and the first positions equal to it, so that the output is in
+// ascending position order.  Rows of up to CACHE_KEYS scores keep their keys
+// in shared memory; longer rows are read again from global memory (L2) on
+// every pass.
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
 namespace sa {
 namespace topk {
 
-constexpr int THREADS = 256;
+constexpr int THREADS = 256, WARPS = THREADS / 32;
 constexpr int CACHE_KEYS = 16384;   // 64 KB of keys in shared memory
+constexpr int BATCH = 16;           // scores a thread loads before it uses any of them
 
 // Order-preserving key of an fp32 score (larger score -> larger key, equal
 // scores -> equal keys, so -0 and +0 tie as they compare equal); 0 for scores
-// that are never selected (-inf, NaN), which no selectable score maps to.
+// that are never selected (-inf, NaN), which no selectable score maps to
+// (every selectable key is at least 0x00800000).
 __device__ __forceinline__ uint32_t key_of(float x)
 {
     if (x != x || x == -INFINITY)
@@ -51,108 +59,169 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int &total)
         warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int s = lane < THREADS / 32 ? warp_sums[lane] : 0;
+        int s = lane < WARPS ? warp_sums[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, s, o);
             if (lane >= o)
                 s += y;
         }
-        if (lane < THREADS / 32)
+        if (lane < WARPS)
             warp_sums[lane] = s;
     }
     __syncthreads();
-    total = warp_sums[THREADS / 32 - 1];
+    total = warp_sums[WARPS - 1];
     const int before = warp > 0 ? warp_sums[warp - 1] : 0;
     __syncthreads();
     return before + x;
 }
+
+// hist[bin] += 1 for every lane with `active` (whole warp calls): lanes with
+// the same bin add together.
+__device__ __forceinline__ void hist_add(int *hist, uint32_t bin, bool active, int lane)
+{
+    const unsigned act = __ballot_sync(0xffffffffu, active);
+    if (active) {
+        const unsigned same = __match_any_sync(act, bin);
+        if (lane == __ffs(same) - 1)
+            atomicAdd(&hist[bin], __popc(same));
+    }
+}
+
+static_assert(THREADS == 256, "one thread per histogram bin");
 
 __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
                                                        int L, int k, int offset, int32_t *__restrict__ out)
 {
     extern __shared__ uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
     __shared__ int hist[256];
-    __shared__ int warp_sums[THREADS / 32];
-    __shared__ uint32_t sel_prefix, sel_mask;
-    __shared__ int sel_remaining, n_valid;
+    __shared__ int warp_sums[WARPS];
+    __shared__ int wcount[2][WARPS];
+    __shared__ uint32_t sel_prefix;
+    __shared__ int sel_remaining;
     const int64_t row = blockIdx.x;
     const float *src = scores + row * row_stride;
     int32_t *dst = out + row * (int64_t)k;
     const bool cached = L <= CACHE_KEYS;
-    const int t = threadIdx.x;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     auto key_at = [&](int j) -> uint32_t { return cached ? cache[j] : key_of(__ldg(src + j)); };
 
-    // keys (into shared memory when they fit) and the number of selectable positions
-    int nv = 0;
-    for (int j = t; j < L; j += THREADS) {
-        const uint32_t kk = key_of(__ldg(src + j));
-        if (cached)
-            cache[j] = kk;
-        nv += kk != 0u;
-    }
-    int total = 0;
-    block_scan(nv, warp_sums, total);
-    if (t == 0) {
-        n_valid = total;
-        sel_prefix = 0u;
-        sel_mask = 0u;
-        sel_remaining = k;
-    }
+    // keys (into shared memory when they fit), the number of selectable
+    // positions and the histogram of their top byte
+    hist[t] = 0;
     __syncthreads();
-    const int valid = n_valid;
-
-    // threshold: the k-th largest key (or the smallest selectable one when
-    // there are no more than k); sel_remaining = how many keys equal to it are taken
-    if (valid > k) {
-        for (int pass = 3; pass >= 0; --pass) {
-            for (int i = t; i < 256; i += THREADS)
-                hist[i] = 0;
-            __syncthreads();
-            const uint32_t prefix = sel_prefix, mask = sel_mask;
-            const int shift = 8 * pass;
-            for (int j = t; j < L; j += THREADS) {
-                const uint32_t kk = key_at(j);
-                if (kk != 0u && (kk & mask) == prefix)
-                    atomicAdd(&hist[(kk >> shift) & 255u], 1);
-            }
-            __syncthreads();
-            if (t == 0) {
-                int need = sel_remaining, b = 255;
-                for (; b > 0; --b) {
-                    if (hist[b] >= need)
-                        break;
-                    need -= hist[b];
-                }
-                sel_prefix = prefix | ((uint32_t)b << shift);
-                sel_mask = mask | (0xFFu << shift);
-                sel_remaining = need;
-            }
-            __syncthreads();
+    int nv = 0;
+    for (int base = 0; base < L; base += THREADS * BATCH) {
+        float v[BATCH];
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int j = base + THREADS * u + t;
+            v[u] = j < L ? __ldg(src + j) : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < BATCH; ++u) {
+            const int j = base + THREADS * u + t;
+            const uint32_t kk = key_of(v[u]);   // 0 past the end
+            if (cached && j < L)
+                cache[j] = kk;
+            nv += kk != 0u;
+            hist_add(hist, kk >> 24, kk != 0u, lane);
         }
     }
-    const uint32_t thr = valid > k ? sel_prefix : 1u;   // 1: every selectable key is taken
-    const int take_eq = valid > k ? sel_remaining : L;
+    int valid = 0;
+    block_scan(nv, warp_sums, valid);
 
-    // ordered pass: positions above the threshold, then the first take_eq equal to it
-    int written = 0, eq_seen = 0;
-    for (int base = 0; base < L; base += THREADS) {
-        const int j = base + t;
-        const uint32_t kk = j < L ? key_at(j) : 0u;
-        const int is_gt = kk > thr ? 1 : 0;
-        const int is_eq = (kk == thr && kk != 0u) ? 1 : 0;
-        int eq_total = 0;
-        const int eq_rank = block_scan(is_eq, warp_sums, eq_total) - is_eq + eq_seen;
-        const int take = is_gt | (is_eq & (eq_rank < take_eq ? 1 : 0));
-        int take_total = 0;
-        const int pos = block_scan(take, warp_sums, take_total) - take + written;
-        if (take && pos < k)
-            dst[pos] = j + offset;
-        written += take_total;
-        eq_seen += eq_total;
+    // threshold: the k-th largest key and how many keys equal to it are taken;
+    // with no more than k selectable keys, all of them (threshold 1, below
+    // every selectable key)
+    uint32_t thr = 1u;
+    int take_eq = 0;
+    if (valid > k) {
+        uint32_t prefix = 0u, mask = 0u;
+        int need = k;
+        for (int pass = 3; pass >= 0; --pass) {
+            const int shift = 8 * pass;
+            if (pass < 3) {
+                hist[t] = 0;
+                __syncthreads();
+                for (int base = 0; base < L; base += THREADS * BATCH) {
+                    uint32_t kb[BATCH];
+#pragma unroll
+                    for (int u = 0; u < BATCH; ++u) {
+                        const int j = base + THREADS * u + t;
+                        kb[u] = j < L ? key_at(j) : 0u;
+                    }
+                    // below the top byte the keys that share a prefix spread over
+                    // the bins: plain atomics
+#pragma unroll
+                    for (int u = 0; u < BATCH; ++u)
+                        if (kb[u] != 0u && (kb[u] & mask) == prefix)
+                            atomicAdd(&hist[(kb[u] >> shift) & 255u], 1);
+                }
+                __syncthreads();
+            }
+            // thread i holds bin 255 - i: the running count from the top first
+            // reaches `need` in the bin of the need-th largest key
+            const int c = hist[255 - t];
+            int tot = 0;
+            const int cum = block_scan(c, warp_sums, tot);
+            if (cum >= need && cum - c < need) {
+                sel_prefix = prefix | ((uint32_t)(255 - t) << shift);
+                sel_remaining = need - (cum - c);
+            }
+            __syncthreads();
+            prefix = sel_prefix;
+            need = sel_remaining;
+            mask |= 0xFFu << shift;
+            __syncthreads();
+        }
+        thr = prefix;
+        take_eq = need;
     }
-    const int n_out = written < k ? written : k;
-    for (int i = n_out + t; i < k; i += THREADS)
+
+    // ordered pass: warp w takes positions [w0, w1), a multiple of 32 wide
+    const int per = ((L + WARPS - 1) / WARPS + 31) & ~31;
+    const int w0 = min(L, warp * per), w1 = min(L, w0 + per);
+    int gt = 0, eq = 0;
+    for (int base = w0; base < w1; base += 32) {
+        const int j = base + lane;
+        const uint32_t kk = j < w1 ? key_at(j) : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, kk > thr));
+        eq += __popc(__ballot_sync(0xffffffffu, kk == thr && kk != 0u));
+    }
+    if (lane == 0) {
+        wcount[0][warp] = gt;
+        wcount[1][warp] = eq;
+    }
+    __syncthreads();
+    int gt_before = 0, eq_before = 0, gt_all = 0, eq_all = 0;
+#pragma unroll
+    for (int i = 0; i < WARPS; ++i) {
+        gt_before += i < warp ? wcount[0][i] : 0;
+        eq_before += i < warp ? wcount[1][i] : 0;
+        gt_all += wcount[0][i];
+        eq_all += wcount[1][i];
+    }
+    int pos = gt_before + min(eq_before, take_eq);
+    int eq_seen = eq_before;
+    const unsigned below = (1u << lane) - 1u;
+    for (int base = w0; base < w1; base += 32) {
+        const int j = base + lane;
+        const uint32_t kk = j < w1 ? key_at(j) : 0u;
+        const bool is_eq = kk == thr && kk != 0u;
+        const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
+        const bool take = kk > thr || (is_eq && eq_seen + __popc(eqm & below) < take_eq);
+        const unsigned tm = __ballot_sync(0xffffffffu, take);
+        if (take) {
+            const int o = pos + __popc(tm & below);
+            if (o < k)
+                dst[o] = j + offset;
+        }
+        pos += __popc(tm);
+        eq_seen += __popc(eqm);
+    }
+    const int taken = gt_all + min(eq_all, take_eq);
+    for (int i = min(taken, k) + t; i < k; i += THREADS)
         dst[i] = -1;
 }
 
