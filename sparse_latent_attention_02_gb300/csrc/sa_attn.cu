@@ -27,8 +27,8 @@
 //     double-buffered shared list and, when kv is larger than L2, warms L2
 //     with the next segment's rows; warp 25 allocates TMEM and issues the
 //     MMAs (one elected lane); warps 26-27 only complete the last
-//     warpgroup.  setmaxnreg gives the softmax warps 128 registers per
-//     thread, the gather warps 48 and the last warpgroup 56.
+//     warpgroup.  setmaxnreg gives the softmax warps 112 registers per
+//     thread, the gather warps 56 and the last warpgroup 56.
 //   * Online softmax in base 2 with the sink as the starting maximum and a
 //     lazy rescale: the running maximum moves only when a score exceeds it by
 //     more than 2^8, so O^T in TMEM is almost never rewritten.  Row sums are
@@ -55,9 +55,9 @@ constexpr int WARP_CONTROL = WARP_GATHER0 + NUM_GATHER_WARPS, WARP_MMA = WARP_CO
 // warpgroups (warps 26, 27 have no role and only lend registers).
 constexpr int THREADS = 28 * 32;                // 896
 // Register split (setmaxnreg, per warpgroup): the launch gives every thread
-// 72; the softmax warps take 128, the gather warps keep 48 and the last
-// warpgroup (control, MMA) 56: 256*128 + 512*48 + 128*56 = 896*72.
-constexpr int REGS_SOFTMAX = 128, REGS_GATHER = 48, REGS_LAST = 56, REGS_LAUNCH = 72;
+// 72; the softmax warps take 112, the gather warps 56 and the last
+// warpgroup (control, MMA) 56: 256*112 + 512*56 + 128*56 = 896*72.
+constexpr int REGS_SOFTMAX = 112, REGS_GATHER = 56, REGS_LAST = 56, REGS_LAUNCH = 72;
 constexpr int GATHER_THREADS = NUM_GATHER_WARPS * 32, LAST_THREADS = THREADS - SMX_THREADS - GATHER_THREADS;
 static_assert(THREADS % 128 == 0 && NUM_SOFTMAX_WARPS % 4 == 0, "setmaxnreg acts on whole warpgroups");
 static_assert(THREADS >= (WARP_MMA + 1) * 32, "every role has a warp");
