@@ -38,8 +38,8 @@ HEADLINE = "decode"
 KERNEL_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)),
                           "sparse_latent_attention_02_gb300", "csrc", "sa_attn.cu")
 MEASURED_TRAFFIC = {
-    "decode": ("4ab438e0c373c63c6f1b96810608c4320779ceb8c358e539b76ee989d3a23e16", 47_199_232),
-    "prefill": ("4ab438e0c373c63c6f1b96810608c4320779ceb8c358e539b76ee989d3a23e16", 1_058_521_856),
+    "decode": ("8a28ecad73c967ea49d4c0ff9df5dbfe5b915f0ac69b36eaa917b2be1c305ec5", 46_795_520),
+    "prefill": ("8a28ecad73c967ea49d4c0ff9df5dbfe5b915f0ac69b36eaa917b2be1c305ec5", 1_056_809_472),
 }
 
 
@@ -489,6 +489,14 @@ def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict) -> dict:
                          "peak_note": f"{pk['source']} sustained bf16 (the products are bf16)"}}
 
 
+# the additional lines that are not attention workloads, by name
+EXTRA_LINES = {
+    "topk": lambda steps, warmup, dev, pk: bench_topk(steps, warmup, dev, pk),
+    "decode_fp4": lambda steps, warmup, dev, pk: bench_decode_fp4(steps, warmup, dev, pk),
+    "fused_tail_fp8": lambda steps, warmup, dev, pk: bench_fused_tail_fp8(steps, warmup, dev, pk),
+}
+
+
 def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
     """The fp64 oracle, as it stands, on the host cores: whole decode steps
     (all queries of one input set) repeated until about `budget_s` seconds."""
@@ -626,9 +634,19 @@ def main():
     ap.add_argument("--sets", type=int, default=None,
                     help="number of rotating input sets (default: enough for > 2x L2)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--extra", choices=sorted(EXTRA_LINES),
+                    help="time only this additional line (one GPU) and print it as JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.extra:
+        import sparse_latent_attention_02_gb300 as sa
+        sa.build()
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps({"extra": args.extra,
+                          **EXTRA_LINES[args.extra](args.steps, args.warmup, dev, peaks())}))
+        return
     rank, world, local = dist_env()
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks exit at once
