@@ -687,8 +687,9 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 
 // Split schedule: the P pieces of one query's list run as one cluster, and
 // CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  Every
-// CTA sends each peer its unnormalised O^T columns and its (m, l) for that
-// peer's heads into the peer's chunk buffer: it stages them in its own slot
+// CTA sends each peer its unnormalised O^T columns (scaled by row_scale(l),
+// as fp16 pairs of adjacent heads) and its (m, l) for that peer's heads into
+// the peer's chunk buffer: it stages them in its own slot
 // of its own chunk buffer (the slot no peer writes) and moves them with one
 // bulk shared-to-shared copy per peer, which completes on the peer's XFULL
 // barrier.  A CTA offers its buffer (arrives on each peer's XRDY barrier)
