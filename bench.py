@@ -38,8 +38,8 @@ HEADLINE = "decode"
 KERNEL_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)),
                           "sparse_latent_attention_02_gb300", "csrc", "sa_attn.cu")
 MEASURED_TRAFFIC = {
-    "decode": ("8a28ecad73c967ea49d4c0ff9df5dbfe5b915f0ac69b36eaa917b2be1c305ec5", 46_795_520),
-    "prefill": ("8a28ecad73c967ea49d4c0ff9df5dbfe5b915f0ac69b36eaa917b2be1c305ec5", 1_056_809_472),
+    "decode": ("f093ba96370f5f0dbb91c54c752a0635227b629290b4d88e9bbcb3bb73438a98", 46_795_520),
+    "prefill": ("f093ba96370f5f0dbb91c54c752a0635227b629290b4d88e9bbcb3bb73438a98", 1_056_809_472),
 }
 
 
