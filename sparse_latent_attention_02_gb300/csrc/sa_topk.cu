@@ -12,8 +12,8 @@
 // One CTA per row.  Scores become order-preserving 32-bit keys; a four-pass
 // radix select (8 bits per pass, most significant first) finds the k-th
 // largest key: each pass histograms the keys that share the prefix chosen so
-// far (in the first pass, where a few bins take most keys, lanes of a warp
-// that hit the same bin add together) and a block-wide scan over the bins, largest
+// far (the first pass, where a few bins take most keys, into one histogram
+// per warp, summed afterwards) and a block-wide scan over the bins, largest
 // first, picks the bin that holds the k-th key.  The first pass is folded
 // into the pass that computes the keys.  The ordered pass gives each warp a
 // contiguous range of positions: the warps count their keys above the
@@ -76,18 +76,6 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int &total)
     return before + x;
 }
 
-// hist[bin] += 1 for every lane with `active` (whole warp calls): lanes with
-// the same bin add together.
-__device__ __forceinline__ void hist_add(int *hist, uint32_t bin, bool active, int lane)
-{
-    const unsigned act = __ballot_sync(0xffffffffu, active);
-    if (active) {
-        const unsigned same = __match_any_sync(act, bin);
-        if (lane == __ffs(same) - 1)
-            atomicAdd(&hist[bin], __popc(same));
-    }
-}
-
 static_assert(THREADS == 256, "one thread per histogram bin");
 
 __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
@@ -95,6 +83,7 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
 {
     extern __shared__ uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
     __shared__ int hist[256];
+    __shared__ int whist[WARPS][256];     // first pass: one histogram per warp
     __shared__ int warp_sums[WARPS];
     __shared__ int wcount[2][WARPS];
     __shared__ uint32_t sel_prefix;
@@ -107,8 +96,10 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
     auto key_at = [&](int j) -> uint32_t { return cached ? cache[j] : key_of(__ldg(src + j)); };
 
     // keys (into shared memory when they fit), the number of selectable
-    // positions and the histogram of their top byte
-    hist[t] = 0;
+    // positions and the histogram of their top byte (one per warp, summed)
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w)
+        whist[w][t] = 0;
     __syncthreads();
     int nv = 0;
     for (int base = 0; base < L; base += THREADS * BATCH) {
@@ -125,11 +116,20 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
             if (cached && j < L)
                 cache[j] = kk;
             nv += kk != 0u;
-            hist_add(hist, kk >> 24, kk != 0u, lane);
+            if (kk != 0u)
+                atomicAdd(&whist[warp][kk >> 24], 1);
         }
     }
     int valid = 0;
     block_scan(nv, warp_sums, valid);
+    {
+        int sum = 0;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w)
+            sum += whist[w][t];
+        hist[t] = sum;
+    }
+    __syncthreads();
 
     // threshold: the k-th largest key and how many keys equal to it are taken;
     // with no more than k selectable keys, all of them (threshold 1, below
