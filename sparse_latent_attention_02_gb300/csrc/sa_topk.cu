@@ -78,6 +78,8 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int &total)
 
 static_assert(THREADS == 256, "one thread per histogram bin");
 
+// CACHED: the row's keys stay in shared memory (L <= CACHE_KEYS)
+template <bool CACHED>
 __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
                                                        int L, int k, int offset, int32_t *__restrict__ out)
 {
@@ -91,9 +93,13 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
     const int64_t row = blockIdx.x;
     const float *src = scores + row * row_stride;
     int32_t *dst = out + row * (int64_t)k;
-    const bool cached = L <= CACHE_KEYS;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    auto key_at = [&](int j) -> uint32_t { return cached ? cache[j] : key_of(__ldg(src + j)); };
+    auto key_at = [&](int j) -> uint32_t {
+        if constexpr (CACHED)
+            return cache[j];
+        else
+            return key_of(__ldg(src + j));
+    };
 
     // keys (into shared memory when they fit), the number of selectable
     // positions and the histogram of their top byte (one per warp, summed)
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
         for (int u = 0; u < BATCH; ++u) {
             const int j = base + THREADS * u + t;
             const uint32_t kk = key_of(v[u]);   // 0 past the end
-            if (cached && j < L)
+            if (CACHED && j < L)
                 cache[j] = kk;
             nv += kk != 0u;
             if (kk != 0u)
@@ -232,12 +238,16 @@ cudaError_t launch_topk(const float *scores, int64_t row_stride, int64_t rows, i
 {
     if (rows == 0 || k == 0)
         return cudaSuccess;
-    const size_t smem = L <= topk::CACHE_KEYS ? (size_t)L * 4 : 0;
-    cudaError_t e = cudaFuncSetAttribute(topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(topk::CACHE_KEYS * 4));
-    if (e != cudaSuccess)
-        return e;
-    topk::topk_kernel<<<(unsigned)rows, topk::THREADS, smem, st>>>(scores, row_stride, L, k, offset, out);
+    if (L <= topk::CACHE_KEYS) {
+        cudaError_t e = cudaFuncSetAttribute(topk::topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(topk::CACHE_KEYS * 4));
+        if (e != cudaSuccess)
+            return e;
+        topk::topk_kernel<true><<<(unsigned)rows, topk::THREADS, (size_t)L * 4, st>>>(scores, row_stride, L, k,
+                                                                                     offset, out);
+    } else {
+        topk::topk_kernel<false><<<(unsigned)rows, topk::THREADS, 0, st>>>(scores, row_stride, L, k, offset, out);
+    }
     return cudaGetLastError();
 }
 
