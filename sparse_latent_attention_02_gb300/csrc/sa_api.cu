@@ -199,8 +199,10 @@ sa_status check_attn_args(const void *q, const void *kv, const float *sink, cons
     return SA_OK;
 }
 
-bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
-                    uint32_t box_cols, uint32_t box_rows)
+namespace {
+
+// The driver's cuTensorMapEncodeTiled, looked up once (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
@@ -210,30 +212,39 @@ bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
             qr == cudaDriverEntryPointSuccess)
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
-    if (!g_encode)
+    return g_encode;
+}
+
+}  // namespace
+
+bool encode_tmap_2d(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_cols, uint32_t box_rows)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode)
         return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                        uint32_t box_cols, uint32_t box_rows)
 {
-    CUtensorMap probe;
-    if (!encode_tmap_2d(&probe, base, 1, 64, 64, 1))   // resolves the driver entry point once
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode)
         return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace sa
