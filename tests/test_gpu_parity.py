@@ -489,3 +489,45 @@ def test_fused_tail_fp8_special_weights():
     assert torch.equal(torch.isnan(got), nan)
     assert nan[..., 1 * R + 5].all() and nan[..., 3 * R + 200].all() and nan.sum() == 2 * B * T
     assert torch.equal(got[~nan], ref[~nan])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes_against_oracle(seed):
+    """Seeded random problems across the schedules (whole lists, two to eight
+    list pieces per query, ragged chunks, -1 anywhere, repeated indices): the
+    plain call, the two-source call and the two-source fp4 call against the
+    oracle, and the two-source call against the plain call on the
+    concatenated rows (bit for bit)."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 5))
+    T = int(rng.integers(1, 40))
+    K = int(rng.integers(1, 1025))
+    W = int(rng.integers(0, 200))
+    C = int(rng.integers(1, 1500))
+    N = W + C
+    g = torch.Generator().manual_seed(2000 + seed)
+    q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16)
+    kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16)
+    sink = 2 * torch.randn(64, generator=g)
+    idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
+    idx[torch.rand(B, T, K, generator=g) < float(rng.uniform(0, 0.5))] = -1
+    x = dict(q=q, kv=kv, sink=sink, idx=idx)
+    got = run(x, 512 ** -0.5)
+    ref = full_oracle(x, 512 ** -0.5)
+    compare(got.double().cpu().numpy(), ref, f"random {seed}: B{B} T{T} K{K} N{N}")
+    gd = to_dev(x)
+    two = sa.sparse_attn_two_source(gd["q"], gd["kv"][:, :W].contiguous() if W else None,
+                                    gd["kv"][:, W:].contiguous(), gd["sink"], gd["idx"], 512 ** -0.5,
+                                    W=W, C=C, check=True)
+    assert torch.equal(two, got)
+    # fp4 compressed rows: codes and scales drawn directly
+    codes = torch.randint(0, 256, (B, C, 256), generator=g, dtype=torch.int32).to(torch.uint8)
+    scales = (0x20 + torch.randint(0, 8, (B, C, 32), generator=g, dtype=torch.int32)).to(torch.uint8)
+    win = kv[:, :W].contiguous()
+    got4 = sa.sparse_attn_two_source_fp4(gd["q"], win.cuda() if W else None, codes.cuda(), scales.cuda(),
+                                         gd["sink"], gd["idx"], 512 ** -0.5, W=W, C=C, out_dtype=torch.float32,
+                                         check=True)
+    ref4, bad = oracle.sparse_attn_two_source_fp4(q, win, W, codes.numpy(), scales.numpy(), C, sink, idx,
+                                                  512 ** -0.5)
+    assert bad == 0
+    compare(got4.double().cpu().numpy(), ref4, f"random fp4 {seed}")
