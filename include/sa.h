@@ -186,12 +186,19 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
  * (n = g*R + r; the product rounded to fp32, then to bf16, both to nearest
  * even).  The pages do not give the scale layout; one fp32 scale per
  * 128 x 128 block is taken.
- *   (q ... rope_dim, G, R, out) as for sa_sparse_attn_rope_wo_a; the same
- *          workspace size (sa_sparse_attn_rope_wo_a_workspace_size)
+ *   (q ... rope_dim, G, R, out) as for sa_sparse_attn_rope_wo_a
  *   wo_a_e4m3   E4M3 bytes [G, R, H*D/G] contiguous, 16-byte aligned
  *   wo_a_scales fp32 [G*R/128, H*D/G/128] contiguous, 4-byte aligned
+ *   workspace   sa_sparse_attn_rope_wo_a_fp8_workspace_size bytes: the fused
+ *          call's workspace, plus, with B*T >= 512 tokens, the bf16 copy of
+ *          the weight (R*H*D*2 bytes) that the call decodes into before a
+ *          bf16 grouped GEMM; with fewer tokens the GEMM decodes the weight
+ *          blocks in shared memory (no copy).  The result is the same.
  * H*D/G must be a multiple of 128 (SA_ERR_UNSUPPORTED otherwise).
  */
+size_t sa_sparse_attn_rope_wo_a_fp8_workspace_size(int B, int T, int H, int D, int K,
+                                                   int G, int R);
+
 sa_status sa_sparse_attn_rope_wo_a_fp8(const void *q, const void *kv, const float *sink,
                                        const int32_t *idx, float scale, int B, int T,
                                        int H, int D, int N, int K,

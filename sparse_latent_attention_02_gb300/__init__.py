@@ -21,7 +21,7 @@ from ._build import LIB as _LIB_PATH, build  # noqa: F401
 __all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_two_source_fp4", "sparse_attn_rope_wo_a",
            "sparse_attn_block_tail",
            "topk_indices", "rope_table", "workspace_size",
-           "fused_workspace_size", "check_errors", "SAError", "library", "build"]
+           "fused_workspace_size", "fused_fp8_workspace_size", "check_errors", "SAError", "library", "build"]
 
 HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
 _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_WORKSPACE",
@@ -30,7 +30,8 @@ EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_tw
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
            "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail",
-           "sa_topk_indices", "sa_sparse_attn_two_source_fp4", "sa_sparse_attn_rope_wo_a_fp8")
+           "sa_topk_indices", "sa_sparse_attn_two_source_fp4", "sa_sparse_attn_rope_wo_a_fp8",
+           "sa_sparse_attn_rope_wo_a_fp8_workspace_size")
 
 
 class SAError(RuntimeError):
@@ -68,6 +69,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
             lib.sa_sparse_attn_rope_wo_a.restype = I
             lib.sa_sparse_attn_rope_wo_a.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, I, I,
                                                      V, V, Z, V]
+            lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size.restype = Z
+            lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size.argtypes = [I, I, I, I, I, I, I]
             lib.sa_sparse_attn_rope_wo_a_fp8.restype = I
             lib.sa_sparse_attn_rope_wo_a_fp8.argtypes = [V, V, V, V, F, I, I, I, I, I, I, V, I, V, V, I,
                                                          I, V, V, Z, V]
@@ -140,6 +143,10 @@ def workspace_size(B: int, T: int, K: int) -> int:
 
 def fused_workspace_size(B: int, T: int, K: int, G: int, R: int) -> int:
     return int(library().sa_sparse_attn_rope_wo_a_workspace_size(B, T, HEADS, HEAD_DIM, K, G, R))
+
+
+def fused_fp8_workspace_size(B: int, T: int, K: int, G: int, R: int) -> int:
+    return int(library().sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, HEADS, HEAD_DIM, K, G, R))
 
 
 def _attn_args(q, kv, sink, idx):
@@ -379,9 +386,9 @@ def sparse_attn_rope_wo_a_fp8(q: torch.Tensor, kv: torch.Tensor, sink: torch.Ten
     else:
         _need(out, "out", torch.bfloat16, 3)
     lib = library()
-    need = int(lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, H, D, K, G, R))
     if workspace is None:
-        workspace = _workspace(need, q.device, "fused")
+        need = int(lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, H, D, K, G, R))
+        workspace = _workspace(need, q.device, "fused_fp8")
     code = lib.sa_sparse_attn_rope_wo_a_fp8(q.data_ptr(), kv.data_ptr(), sink.data_ptr(),
                                             idx.data_ptr(), float(scale), B, T, H, D, N, K,
                                             rope_cos_sin.data_ptr(), rope_dim, wo_a_e4m3.data_ptr(),

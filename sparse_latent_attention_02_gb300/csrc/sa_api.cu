@@ -381,6 +381,12 @@ size_t sa_sparse_attn_rope_wo_a_workspace_size(int B, int T, int H, int D, int K
 
 namespace {
 
+// fp8 wo_a: with at least this many tokens the weight is decoded into a bf16
+// workspace copy before a bf16 GEMM; below it the GEMM decodes the weight
+// blocks in shared memory (measured on GB300: the GEMM-side decoding is
+// faster at 64 and 256 tokens, the copy from 1024 tokens on).
+constexpr int64_t FP8_DECODE_FIRST_TOKENS = 512;
+
 // Host checks of the tail arguments.  rope_dim is a multiple of 32 so that
 // every warp of the epilogue either rotates all of its 32 features or none.
 // fp8 weights (fp8 true): whole 128 x 128 scale blocks and 4-byte aligned scales.
@@ -483,10 +489,29 @@ sa_status sa_sparse_attn_rope_wo_a_fp8(const void *q, const void *kv, const floa
         return SA_ERR_CUDA;
     const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
     const size_t o_bytes = round256((size_t)BT * H * D * 2);
-    if (ws_bytes < attn_ws + o_bytes)
+    const bool decode_first = BT >= FP8_DECODE_FIRST_TOKENS;
+    const size_t w_bytes = decode_first ? round256((size_t)R * H * D * 2) : 0;   // bf16 copy of wo_a
+    if (ws_bytes < attn_ws + o_bytes + w_bytes)
         return SA_ERR_WORKSPACE;
-    return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a_e4m3,
-                          wo_a_scales, G, R, out, workspace, attn_ws, sms, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!decode_first)   // few tokens: the GEMM decodes the weight blocks itself
+        return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a_e4m3,
+                              wo_a_scales, G, R, out, workspace, attn_ws, sms, s);
+    // many tokens: the weight is decoded once into a bf16 copy in the workspace
+    // (one bandwidth-bound pass) and the grouped GEMM runs on bf16 operands
+    uint16_t *w16 = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) + attn_ws + o_bytes);
+    if (launch_dequant_fp8(wo_a_e4m3, wo_a_scales, w16, G * R, H * D / G, sms, s) != cudaSuccess)
+        return SA_ERR_CUDA;
+    return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, w16, nullptr, G, R,
+                          out, workspace, attn_ws, sms, s);
+}
+
+size_t sa_sparse_attn_rope_wo_a_fp8_workspace_size(int B, int T, int H, int D, int K, int G, int R)
+{
+    const size_t fused = sa_sparse_attn_rope_wo_a_workspace_size(B, T, H, D, K, G, R);
+    if (B < 0 || T < 0 || H < 0 || D < 0 || R < 0 || (int64_t)B * T < FP8_DECODE_FIRST_TOKENS)
+        return fused;
+    return round256(fused) + round256((size_t)R * H * D * 2);
 }
 
 size_t sa_sparse_attn_block_tail_workspace_size(int B, int T, int H, int D, int K, int G, int R)

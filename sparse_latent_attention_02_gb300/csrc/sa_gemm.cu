@@ -390,7 +390,43 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
     }
 }
 
+// E4M3 weight [rows, cols] with one fp32 scale per 128 x 128 block -> bf16
+// [rows, cols], each value bf16(fp32(e4m3 * scale)) as in the fused decoders;
+// a thread converts 16 bytes per step (grid-stride).  cols % 128 == 0.
+__global__ void __launch_bounds__(256) dequant_fp8_kernel(const uint8_t *__restrict__ w8,
+                                                          const float *__restrict__ scales,
+                                                          uint16_t *__restrict__ w16, int rows, int cols)
+{
+    const int per_row = cols / 16;
+    const int total = rows * per_row;
+    const int scale_cols = cols / FP8_BLOCK;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int r = i / per_row, c = (i - r * per_row) * 16;
+        const size_t off = (size_t)r * cols + c;
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(w8 + off));
+        const float sc = __ldg(scales + (size_t)(r / FP8_BLOCK) * scale_cols + c / FP8_BLOCK);
+        uint4 lo, hi;
+        dequant_e4m3x16(w, sc, lo, hi);
+        uint4 *dst = reinterpret_cast<uint4 *>(w16 + off);
+        dst[0] = lo;
+        dst[1] = hi;
+    }
+}
+
 }  // namespace gemm
+
+cudaError_t launch_dequant_fp8(const uint8_t *w8, const float *scales, uint16_t *w16, int rows, int cols,
+                               int num_sms, cudaStream_t st)
+{
+    const int64_t total = (int64_t)rows * (cols / 16);
+    if (total <= 0)
+        return cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)num_sms * 8)
+        blocks = (int64_t)num_sms * 8;
+    gemm::dequant_fp8_kernel<<<(unsigned)blocks, 256, 0, st>>>(w8, scales, w16, rows, cols);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st)
 {

@@ -74,6 +74,9 @@ struct GemmParams {
 };
 
 cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st);
+// E4M3 weight [rows, cols] + fp32 128 x 128 block scales -> bf16 [rows, cols].
+cudaError_t launch_dequant_fp8(const uint8_t *w8, const float *scales, uint16_t *w16, int rows, int cols,
+                               int num_sms, cudaStream_t st);
 
 // Top-k selection of positions per row of scores (see sa_topk_indices).
 cudaError_t launch_topk(const float *scores, int64_t row_stride, int64_t rows, int L, int k, int offset,
