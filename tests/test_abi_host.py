@@ -180,3 +180,16 @@ def test_fused_fp8_argument_checks(lib):
     assert call(R=1000) == UNSUPPORTED
     assert call(G=0) == INVALID
     assert call(B=0, q=None, out=None) == OK      # empty problems touch nothing
+
+
+def test_fp8_tail_workspace_size(lib):
+    """Below 512 tokens the fp8 tail needs the bf16 tail's workspace (the GEMM
+    decodes the weight itself); from 512 tokens on, plus the bf16 copy of the
+    weight (R * H * D * 2 bytes) that the call decodes into."""
+    for B, T in [(1, 1), (64, 1), (2, 255), (1, 511)]:
+        assert (lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, 64, 512, 640, 8, 1024)
+                == lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, 64, 512, 640, 8, 1024))
+    for B, T in [(1, 512), (2, 4096)]:
+        base = lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, 64, 512, 640, 8, 1024)
+        got = lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, 64, 512, 640, 8, 1024)
+        assert got == base + 1024 * 64 * 512 * 2 and got % 256 == 0
