@@ -1,0 +1,72 @@
+"""Host-side arithmetic of bench.py (CPU only): the algorithmic work behind
+the roofline figures, the traffic table's source check and the clock summary."""
+import os
+import sys
+import time
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from sparse_latent_attention_02_gb300 import inputs as I  # noqa: E402
+
+
+def test_decode_algorithmic_bytes():
+    """64 queries x (640 rows x 1 KiB + q 64 KiB + bf16 out 64 KiB + 640 int32
+    indices) + the 256-byte sink = 50,495,744 bytes; flops 4*64*512 per
+    (query, row) pair."""
+    wl = I.WORKLOADS["decode"]
+    x = I.make_inputs(wl, seed=0)
+    a = bench.algorithmic(wl, x["idx"])
+    assert a["pairs"] == 64 * 640
+    assert a["bytes"] == 64 * (640 * 1024 + 65536 + 65536 + 640 * 4) + 256 == 50_495_744
+    assert a["flops"] == 4 * 64 * 512 * 64 * 640
+
+
+def test_prefill_flops_count_valid_pairs_only():
+    wl = I.WORKLOADS["prefill"]
+    x = I.make_inputs(wl, seed=0)
+    a = bench.algorithmic(wl, x["idx"])
+    assert a["pairs"] == int((x["idx"] >= 0).sum()) == 4_972_096
+    assert a["flops"] == 4 * 64 * 512 * 4_972_096
+
+
+def test_skipped_entries_are_not_counted():
+    wl = I.WORKLOADS["decode"]
+    x = I.make_inputs(wl, seed=0)
+    idx = x["idx"].clone()
+    idx[:, :, ::2] = -1
+    a, b = bench.algorithmic(wl, x["idx"]), bench.algorithmic(wl, idx)
+    assert b["pairs"] == a["pairs"] // 2
+    assert a["bytes"] - b["bytes"] == (a["pairs"] - b["pairs"]) * 1024
+
+
+def test_traffic_table_is_keyed_to_the_kernel_source(tmp_path, monkeypatch):
+    """A measured traffic figure is reported only for the kernel source it was
+    captured on."""
+    assert bench.measured_traffic("no such workload") is None
+    if bench.measured_traffic("decode") is not None:
+        changed = tmp_path / "sa_attn.cu"
+        changed.write_text(open(bench.KERNEL_SRC).read() + "\n// changed\n")
+        monkeypatch.setattr(bench, "KERNEL_SRC", str(changed))
+        assert bench.measured_traffic("decode") is None
+
+
+def test_clock_summary_inside_window_and_reasons():
+    s = bench.ClockSampler(0)
+    t = time.time()
+    row = lambda mhz, hw="Not Active": [str(mhz), "2070", "900.0", "0x0", hw, "Not Active", "Not Active",
+                                        "Not Active"]
+    s.samples = [(t - 1.0, row(1000)), (t + 0.01, row(2070)), (t + 0.03, row(2055)),
+                 (t + 0.05, row(2070, "Active")), (t + 2.0, row(500))]
+    out = s.summary(t, t + 0.06)
+    assert out["samples"] == 3 and out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["hw_slowdown"]
+    assert "note" not in out
+    # a window with no sample inside falls back to the nearest ones, and says so
+    near = s.summary(t + 0.5, t + 0.51)
+    assert near["samples"] == 3 and "note" in near
+
+
+def test_launch_counts_per_call():
+    assert bench.launches_per_call(I.WORKLOADS["decode"], 148) == 1
+    assert bench.launches_per_call(I.WORKLOADS["fused_tail"], 148) == 2
+    assert bench.launches_per_call(I.WORKLOADS["block_tail"], 148) == 3
