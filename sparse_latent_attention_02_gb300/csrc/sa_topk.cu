@@ -9,19 +9,19 @@
 //   (masked positions), ties to the smaller position; the chosen positions,
 //   in ascending order, plus `offset`; -1 after them when fewer than k exist.
 //
-// One CTA per row.  Scores become order-preserving 32-bit keys; a four-pass
-// radix select (8 bits per pass, most significant first) finds the k-th
+// One CTA per row.  Scores become order-preserving 32-bit keys; a three-pass
+// radix select (11, 11 and 10 bits, most significant first) finds the k-th
 // largest key: each pass histograms the keys that share the prefix chosen so
-// far (the first pass, where a few bins take most keys, into one histogram
-// per warp, summed afterwards) and a block-wide scan over the bins, largest
-// first, picks the bin that holds the k-th key.  The first pass is folded
-// into the pass that computes the keys.  The ordered pass gives each warp a
-// contiguous range of positions: the warps count their keys above the
-// threshold and equal to it, and then write, with ballots, every position
-// above it and the first positions equal to it, so that the output is in
-// ascending position order.  Rows of up to CACHE_KEYS scores keep their keys
-// in shared memory; longer rows are read again from global memory (L2) on
-// every pass.
+// far into 2048 bins, and a block-wide scan over the bins, largest first
+// (eight per thread), picks the bin that holds the k-th key.  The first pass
+// is folded into the pass that computes the keys.  The ordered pass gives each
+// warp a contiguous range of positions, four keys a lane: the warps count
+// their keys above the threshold and equal to it, and then write, after one
+// warp scan of both counts per 128 keys, every position above it and the
+// first positions equal to it, so that the output is in ascending position
+// order.  Rows of up to CACHE_KEYS scores keep their keys in shared memory and
+// read them 16 bytes at a time; longer rows are read again from global memory
+// (L2) on every pass.
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
@@ -31,17 +31,20 @@ namespace topk {
 constexpr int THREADS = 256, WARPS = THREADS / 32;
 constexpr int CACHE_KEYS = 16384;   // 64 KB of keys in shared memory
 constexpr int BATCH = 16;           // scores a thread loads before it uses any of them
+constexpr int BINS = 2048;          // 11-bit digits
+constexpr int SWEEP_VEC = 2;        // groups of four keys a thread loads before it uses any of them
 
 // Order-preserving key of an fp32 score (larger score -> larger key, equal
 // scores -> equal keys, so -0 and +0 tie as they compare equal); 0 for scores
 // that are never selected (-inf, NaN), which no selectable score maps to
-// (every selectable key is at least 0x00800000).
+// (every selectable key is at least 0x00800000).  Adding +0 turns -0 into +0
+// and leaves every other value, subnormals included, as it is (the library
+// is built without flush-to-zero).
 __device__ __forceinline__ uint32_t key_of(float x)
 {
-    if (x != x || x == -INFINITY)
-        return 0u;
-    const uint32_t b = x == 0.0f ? 0u : __float_as_uint(x);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    const uint32_t b = __float_as_uint(x + 0.0f);
+    const uint32_t kk = b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+    return x > -INFINITY ? kk : 0u;
 }
 
 // Inclusive block-wide sum of one int per thread; also returns the total.
@@ -76,20 +79,20 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int &total)
     return before + x;
 }
 
-static_assert(THREADS == 256, "one thread per histogram bin");
+static_assert(THREADS * 8 == BINS, "eight histogram bins per thread");
 
 // CACHED: the row's keys stay in shared memory (L <= CACHE_KEYS)
 template <bool CACHED>
-__global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
+__global__ void __launch_bounds__(THREADS, 8) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
                                                        int L, int k, int offset, int32_t *__restrict__ out)
 {
-    extern __shared__ uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
-    __shared__ int hist[256];
-    __shared__ int whist[WARPS][256];     // first pass: one histogram per warp
+    extern __shared__ __align__(16) uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
+    __shared__ __align__(16) int hist[BINS];
     __shared__ int warp_sums[WARPS];
     __shared__ int wcount[2][WARPS];
     __shared__ uint32_t sel_prefix;
     __shared__ int sel_remaining;
+    __shared__ bool sel_whole;
     const int64_t row = blockIdx.x;
     const float *src = scores + row * row_stride;
     int32_t *dst = out + row * (int64_t)k;
@@ -100,14 +103,32 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
         else
             return key_of(__ldg(src + j));
     };
+    // keys j .. j+3 (j a multiple of 4), 0 from position lim on
+    auto keys4 = [&](int j, int lim, uint32_t *kb) {
+        if constexpr (CACHED) {
+            if (j + 4 <= lim) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(cache + j);
+                kb[0] = v.x;
+                kb[1] = v.y;
+                kb[2] = v.z;
+                kb[3] = v.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    kb[i] = j + i < lim ? cache[j + i] : 0u;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                kb[i] = j + i < lim ? key_of(__ldg(src + j + i)) : 0u;
+        }
+    };
 
     // keys (into shared memory when they fit), the number of selectable
-    // positions and the histogram of their top byte (one per warp, summed)
-#pragma unroll
-    for (int w = 0; w < WARPS; ++w)
-        whist[w][t] = 0;
+    // positions and the histogram of their top 11 bits
+    for (int i = t; i < BINS; i += THREADS)
+        hist[i] = 0;
     __syncthreads();
-    int nv = 0;
     for (int base = 0; base < L; base += THREADS * BATCH) {
         float v[BATCH];
 #pragma unroll
@@ -121,80 +142,109 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
             const uint32_t kk = key_of(v[u]);   // 0 past the end
             if (CACHED && j < L)
                 cache[j] = kk;
-            nv += kk != 0u;
             if (kk != 0u)
-                atomicAdd(&whist[warp][kk >> 24], 1);
+                atomicAdd(&hist[kk >> 21], 1);
         }
-    }
-    int valid = 0;
-    block_scan(nv, warp_sums, valid);
-    {
-        int sum = 0;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w)
-            sum += whist[w][t];
-        hist[t] = sum;
     }
     __syncthreads();
 
-    // threshold: the k-th largest key and how many keys equal to it are taken;
-    // with no more than k selectable keys, all of them (threshold 1, below
-    // every selectable key)
+    // threshold: every key above thr is taken, and the first take_eq keys
+    // equal to it.  With no more than k selectable keys (the histogram's
+    // total), all of them: thr 1, below every selectable key.  A pass whose
+    // chosen bin holds exactly the keys still needed ends the search: thr is
+    // then the largest key below that bin.
     uint32_t thr = 1u;
     int take_eq = 0;
-    if (valid > k) {
+    {
         uint32_t prefix = 0u, mask = 0u;
         int need = k;
-        for (int pass = 3; pass >= 0; --pass) {
-            const int shift = 8 * pass;
-            if (pass < 3) {
-                hist[t] = 0;
+#pragma unroll 1
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
+            const uint32_t dmask = pass < 2 ? 2047u : 1023u;
+            if (pass > 0) {
+                for (int i = t; i < BINS; i += THREADS)
+                    hist[i] = 0;
                 __syncthreads();
-                for (int base = 0; base < L; base += THREADS * BATCH) {
-                    uint32_t kb[BATCH];
+                for (int base = 0; base < L; base += 4 * THREADS * SWEEP_VEC) {
+                    uint32_t kb[4 * SWEEP_VEC];
 #pragma unroll
-                    for (int u = 0; u < BATCH; ++u) {
-                        const int j = base + THREADS * u + t;
-                        kb[u] = j < L ? key_at(j) : 0u;
-                    }
-                    // below the top byte the keys that share a prefix spread over
-                    // the bins: plain atomics
+                    for (int u = 0; u < SWEEP_VEC; ++u)
+                        keys4(base + 4 * (THREADS * u + t), L, kb + 4 * u);
+                    // below the top digit the keys that share a prefix spread over
+                    // the bins: plain atomics (no key of 0 matches: every prefix
+                    // chosen is nonzero)
 #pragma unroll
-                    for (int u = 0; u < BATCH; ++u)
-                        if (kb[u] != 0u && (kb[u] & mask) == prefix)
-                            atomicAdd(&hist[(kb[u] >> shift) & 255u], 1);
+                    for (int u = 0; u < 4 * SWEEP_VEC; ++u)
+                        if ((kb[u] & mask) == prefix)
+                            atomicAdd(&hist[(kb[u] >> shift) & dmask], 1);
                 }
                 __syncthreads();
             }
-            // thread i holds bin 255 - i: the running count from the top first
-            // reaches `need` in the bin of the need-th largest key
-            const int c = hist[255 - t];
+            // thread i holds bins 2047 - 8i down to 2040 - 8i: the running
+            // count from the top first reaches `need` in the bin of the
+            // need-th largest key
+            const int b0 = BINS - 8 - 8 * t;
+            const int4 lo = *reinterpret_cast<const int4 *>(&hist[b0]);
+            const int4 hi = *reinterpret_cast<const int4 *>(&hist[b0 + 4]);
+            const int c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
+            int own = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                own += c[i];
             int tot = 0;
-            const int cum = block_scan(c, warp_sums, tot);
-            if (cum >= need && cum - c < need) {
-                sel_prefix = prefix | ((uint32_t)(255 - t) << shift);
-                sel_remaining = need - (cum - c);
+            const int cum = block_scan(own, warp_sums, tot);
+            if (pass == 0 && tot <= k)   // the block's total: the same in every thread
+                break;
+            if (cum >= need && cum - own < need) {
+                int run = cum - own;
+                bool found = false;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (!found && run + c[i] >= need) {
+                        sel_prefix = prefix | ((uint32_t)(b0 + 7 - i) << shift);
+                        sel_remaining = need - run;
+                        sel_whole = run + c[i] == need;
+                        found = true;
+                    }
+                    run += c[i];
+                }
             }
             __syncthreads();
             prefix = sel_prefix;
             need = sel_remaining;
-            mask |= 0xFFu << shift;
+            mask |= dmask << shift;
+            const bool whole = sel_whole;
             __syncthreads();
+            if (whole) {   // every key of the bin is taken
+                thr = prefix - 1u;
+                take_eq = 0;
+                break;
+            }
+            if (pass == 2) {   // the bin is one key value
+                thr = prefix;
+                take_eq = need;
+            }
         }
-        thr = prefix;
-        take_eq = need;
     }
 
-    // ordered pass: warp w takes positions [w0, w1), a multiple of 32 wide
-    const int per = ((L + WARPS - 1) / WARPS + 31) & ~31;
+    // ordered pass: warp w takes positions [w0, w1), a multiple of 128 wide;
+    // its counts read four consecutive keys a lane
+    const int per = ((L + WARPS - 1) / WARPS + 127) & ~127;
     const int w0 = min(L, warp * per), w1 = min(L, w0 + per);
+    // (no key of 0 equals thr: thr is 1 or a selectable key)
     int gt = 0, eq = 0;
-    for (int base = w0; base < w1; base += 32) {
-        const int j = base + lane;
-        const uint32_t kk = j < w1 ? key_at(j) : 0u;
-        gt += __popc(__ballot_sync(0xffffffffu, kk > thr));
-        eq += __popc(__ballot_sync(0xffffffffu, kk == thr && kk != 0u));
+    for (int base = w0; base < w1; base += 128) {
+        uint32_t kb[4];
+        keys4(base + 4 * lane, w1, kb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            gt += kb[i] > thr;
+            eq += kb[i] == thr;
+        }
     }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
     if (lane == 0) {
         wcount[0][warp] = gt;
         wcount[1][warp] = eq;
@@ -208,23 +258,36 @@ __global__ void __launch_bounds__(THREADS) topk_kernel(const float *__restrict__
         gt_all += wcount[0][i];
         eq_all += wcount[1][i];
     }
+    // writes: lane l takes keys base + l, base + 32 + l, ... so that each
+    // ballot covers 32 consecutive positions; pos counts the positions
+    // written before them, eq_seen the keys equal to thr (the first take_eq
+    // of all are taken)
     int pos = gt_before + min(eq_before, take_eq);
     int eq_seen = eq_before;
     const unsigned below = (1u << lane) - 1u;
-    for (int base = w0; base < w1; base += 32) {
-        const int j = base + lane;
-        const uint32_t kk = j < w1 ? key_at(j) : 0u;
-        const bool is_eq = kk == thr && kk != 0u;
-        const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
-        const bool take = kk > thr || (is_eq && eq_seen + __popc(eqm & below) < take_eq);
-        const unsigned tm = __ballot_sync(0xffffffffu, take);
-        if (take) {
-            const int o = pos + __popc(tm & below);
-            if (o < k)
-                dst[o] = j + offset;
+    for (int base = w0; base < w1; base += 128) {
+        uint32_t kb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = base + 32 * i + lane;
+            kb[i] = j < w1 ? key_at(j) : 0u;
         }
-        pos += __popc(tm);
-        eq_seen += __popc(eqm);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool is_eq = kb[i] == thr;
+            const unsigned eqm = __ballot_sync(0xffffffffu, is_eq);
+            bool take = kb[i] > thr;
+            if (eqm != 0u)   // the same in every lane
+                take = take || (is_eq && eq_seen + __popc(eqm & below) < take_eq);
+            const unsigned tm = __ballot_sync(0xffffffffu, take);
+            if (take) {
+                const int o = pos + __popc(tm & below);
+                if (o < k)
+                    dst[o] = base + 32 * i + lane + offset;
+            }
+            pos += __popc(tm);
+            eq_seen += __popc(eqm);
+        }
     }
     const int taken = gt_all + min(eq_all, take_eq);
     for (int i = min(taken, k) + t; i < k; i += THREADS)

@@ -317,6 +317,10 @@ def test_block_tail_workload_sampled():
     (32, 1000, 512, "ties"),      # many equal scores: ties go to the smaller position
     (16, 300, 512, "masked"),     # NaN and -inf, fewer than k positions to choose
     (4, 0, 16, "empty"),          # no positions at all
+    (24, 1030, 64, "narrow"),     # scores a few ulps apart and signed zeros: the low digits decide
+    (24, 1030, 64, "tiny"),       # subnormals, signed zeros and -inf: subnormals are not zero
+    (4, 16383, 512, "full"),      # the longest row whose keys stay in shared memory
+    (4, 16385, 512, "full"),      # the shortest row read again from L2 on every pass
 ])
 def test_topk_matches_oracle(rows, L, k, mode):
     """The top-k selection is exact: the same int32 positions, in the same
@@ -328,6 +332,14 @@ def test_topk_matches_oracle(rows, L, k, mode):
             s[r, (r * L) // rows + 1:] = float("-inf")
     elif mode == "ties":
         s = torch.round(s * 4) / 4
+    elif mode == "narrow":
+        s = 1.0 + torch.randint(0, 3, (rows, L), generator=g).double() * 2.0 ** -23
+        s = s.float()
+        s[:, ::7] = -0.0
+        s[:, 1::7] = 0.0
+    elif mode == "tiny":
+        vals = torch.tensor([-1e-40, -0.0, 0.0, 1e-45, 1e-40, 2e-40, float("-inf")])
+        s = vals[torch.randint(0, len(vals), (rows, L), generator=g)]
     elif mode == "masked":
         s[torch.rand(rows, L, generator=g) < 0.1] = float("nan")
         s[torch.rand(rows, L, generator=g) < 0.2] = float("-inf")
