@@ -13,15 +13,16 @@
 // radix select (11, 11 and 10 bits, most significant first) finds the k-th
 // largest key: each pass histograms the keys that share the prefix chosen so
 // far into 2048 bins, and a block-wide scan over the bins, largest first
-// (eight per thread), picks the bin that holds the k-th key.  The first pass
-// is folded into the pass that computes the keys.  The ordered pass gives each
-// warp a contiguous range of positions, four keys a lane: the warps count
-// their keys above the threshold and equal to it, and then write, after one
-// warp scan of both counts per 128 keys, every position above it and the
-// first positions equal to it, so that the output is in ascending position
-// order.  Rows of up to CACHE_KEYS scores keep their keys in shared memory and
-// read them 16 bytes at a time; longer rows are read again from global memory
-// (L2) on every pass.
+// (eight per thread), picks the bin that holds the k-th key; the search ends
+// early once that bin is taken whole.  The first pass is folded into the
+// pass that computes the keys, which also finds the last selectable
+// position: the later passes stop there.  The ordered pass gives each warp a
+// contiguous range of positions: the warps count their keys above the
+// threshold and equal to it, and then write, with ballots over 32 positions
+// at a time, every position above it and the first positions equal to it, so
+// that the output is in ascending position order.  Rows of up to CACHE_KEYS
+// scores keep their keys in shared memory; longer rows are read again from
+// global memory (L2) on every pass.
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
@@ -33,6 +34,7 @@ constexpr int CACHE_KEYS = 16384;   // 64 KB of keys in shared memory
 constexpr int BATCH = 16;           // scores a thread loads before it uses any of them
 constexpr int BINS = 2048;          // 11-bit digits
 constexpr int SWEEP_VEC = 2;        // groups of four keys a thread loads before it uses any of them
+constexpr int VBATCH = 4;           // groups of four scores a thread loads before it uses any of them
 
 // Order-preserving key of an fp32 score (larger score -> larger key, equal
 // scores -> equal keys, so -0 and +0 tie as they compare equal); 0 for scores
@@ -83,7 +85,7 @@ static_assert(THREADS * 8 == BINS, "eight histogram bins per thread");
 
 // CACHED: the row's keys stay in shared memory (L <= CACHE_KEYS)
 template <bool CACHED>
-__global__ void __launch_bounds__(THREADS, 8) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
+__global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
                                                        int L, int k, int offset, int32_t *__restrict__ out)
 {
     extern __shared__ __align__(16) uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
@@ -93,6 +95,7 @@ __global__ void __launch_bounds__(THREADS, 8) topk_kernel(const float *__restric
     __shared__ uint32_t sel_prefix;
     __shared__ int sel_remaining;
     __shared__ bool sel_whole;
+    __shared__ int last_valid;
     const int64_t row = blockIdx.x;
     const float *src = scores + row * row_stride;
     int32_t *dst = out + row * (int64_t)k;
@@ -124,29 +127,81 @@ __global__ void __launch_bounds__(THREADS, 8) topk_kernel(const float *__restric
         }
     };
 
-    // keys (into shared memory when they fit), the number of selectable
-    // positions and the histogram of their top 11 bits
+    // keys (into shared memory when they fit), the histogram of their top 11
+    // bits and the last selectable position: the later passes stop after it
+    // (a causal row ends in masked positions).  A thread visits its
+    // positions in increasing order, so the last one it saw is its largest.
     for (int i = t; i < BINS; i += THREADS)
         hist[i] = 0;
+    if (t == 0)
+        last_valid = -1;
     __syncthreads();
-    for (int base = 0; base < L; base += THREADS * BATCH) {
-        float v[BATCH];
+    int last = -1;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0u) {
+        // 16-byte aligned row: four scores a load
+        constexpr int VB = CACHED ? VBATCH : VBATCH / 2;   // the uncached kernel has fewer registers to spare
+        for (int base = 0; base < L; base += 4 * THREADS * VB) {
+            float4 v[VB];
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int j = base + THREADS * u + t;
-            v[u] = j < L ? __ldg(src + j) : -INFINITY;
+            for (int u = 0; u < VB; ++u) {
+                const int j = base + 4 * (THREADS * u + t);
+                if (j + 4 <= L) {
+                    v[u] = __ldg(reinterpret_cast<const float4 *>(src + j));
+                } else {
+                    v[u].x = j < L ? __ldg(src + j) : -INFINITY;
+                    v[u].y = j + 1 < L ? __ldg(src + j + 1) : -INFINITY;
+                    v[u].z = j + 2 < L ? __ldg(src + j + 2) : -INFINITY;
+                    v[u].w = -INFINITY;   // j + 3 >= L here
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < VB; ++u) {
+                const int j = base + 4 * (THREADS * u + t);
+                const uint32_t kk[4] = {key_of(v[u].x), key_of(v[u].y), key_of(v[u].z), key_of(v[u].w)};
+                if (CACHED) {
+                    if (j + 4 <= L) {
+                        *reinterpret_cast<uint4 *>(cache + j) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (j + i < L)
+                                cache[j + i] = kk[i];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (kk[i] != 0u) {   // 0 past the end
+                        atomicAdd(&hist[kk[i] >> 21], 1);
+                        last = j + i;
+                    }
+            }
         }
+    } else {
+        for (int base = 0; base < L; base += THREADS * BATCH) {
+            float v[BATCH];
 #pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-            const int j = base + THREADS * u + t;
-            const uint32_t kk = key_of(v[u]);   // 0 past the end
-            if (CACHED && j < L)
-                cache[j] = kk;
-            if (kk != 0u)
-                atomicAdd(&hist[kk >> 21], 1);
+            for (int u = 0; u < BATCH; ++u) {
+                const int j = base + THREADS * u + t;
+                v[u] = j < L ? __ldg(src + j) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < BATCH; ++u) {
+                const int j = base + THREADS * u + t;
+                const uint32_t kk = key_of(v[u]);   // 0 past the end
+                if (CACHED && j < L)
+                    cache[j] = kk;
+                if (kk != 0u) {
+                    atomicAdd(&hist[kk >> 21], 1);
+                    last = j;
+                }
+            }
         }
     }
+    last = __reduce_max_sync(0xffffffffu, last);
+    if (lane == 0)
+        atomicMax(&last_valid, last);
     __syncthreads();
+    const int Lv = last_valid + 1;   // positions from Lv on are all masked
 
     // threshold: every key above thr is taken, and the first take_eq keys
     // equal to it.  With no more than k selectable keys (the histogram's
@@ -166,11 +221,11 @@ __global__ void __launch_bounds__(THREADS, 8) topk_kernel(const float *__restric
                 for (int i = t; i < BINS; i += THREADS)
                     hist[i] = 0;
                 __syncthreads();
-                for (int base = 0; base < L; base += 4 * THREADS * SWEEP_VEC) {
+                for (int base = 0; base < Lv; base += 4 * THREADS * SWEEP_VEC) {
                     uint32_t kb[4 * SWEEP_VEC];
 #pragma unroll
                     for (int u = 0; u < SWEEP_VEC; ++u)
-                        keys4(base + 4 * (THREADS * u + t), L, kb + 4 * u);
+                        keys4(base + 4 * (THREADS * u + t), Lv, kb + 4 * u);
                     // below the top digit the keys that share a prefix spread over
                     // the bins: plain atomics (no key of 0 matches: every prefix
                     // chosen is nonzero)
@@ -228,10 +283,10 @@ __global__ void __launch_bounds__(THREADS, 8) topk_kernel(const float *__restric
         }
     }
 
-    // ordered pass: warp w takes positions [w0, w1), a multiple of 128 wide;
-    // its counts read four consecutive keys a lane
-    const int per = ((L + WARPS - 1) / WARPS + 127) & ~127;
-    const int w0 = min(L, warp * per), w1 = min(L, w0 + per);
+    // ordered pass over the positions before Lv: warp w takes [w0, w1), a
+    // multiple of 128 wide; its counts read four consecutive keys a lane
+    const int per = ((Lv + WARPS - 1) / WARPS + 127) & ~127;
+    const int w0 = min(Lv, warp * per), w1 = min(Lv, w0 + per);
     // (no key of 0 equals thr: thr is 1 or a selectable key)
     int gt = 0, eq = 0;
     for (int base = w0; base < w1; base += 128) {

@@ -349,6 +349,24 @@ def test_topk_matches_oracle(rows, L, k, mode):
     assert np.array_equal(got.cpu().numpy(), ref)
 
 
+def test_topk_unaligned_rows():
+    """Rows cut from a wider tensor start on and off 16-byte boundaries, so
+    both load paths of the first pass run in one launch; each row ends in a
+    masked tail of its own length, one row is masked throughout."""
+    g = torch.Generator().manual_seed(77)
+    rows, L, k = 48, 2051, 300
+    big = torch.randn(rows, L + 1, generator=g)
+    for r in range(rows):
+        big[r, 1 + (r * 97) % L:] = float("-inf")
+    big[5, :] = float("-inf")
+    s = big.cuda()[:, 1:]
+    assert s.stride(0) == L + 1
+    got = sa.topk_indices(s, k, offset=7)
+    torch.cuda.synchronize()
+    ref = oracle.topk_indices(big[:, 1:].contiguous().numpy(), k, offset=7)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("B,T,K,W,C,host_c", [
     (4, 1, 640, 128, 4096, False),    # decode shape, split schedule
     (1, 40, 300, 128, 600, False),    # whole queries per CTA
