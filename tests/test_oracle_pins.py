@@ -425,6 +425,21 @@ def test_topk_signed_zeros_tie():
     assert oracle.topk_indices(row[None, :], 3)[0].tolist() == [0, 1, 4]
 
 
+def test_topk_subnormals_are_not_zero():
+    """fp32 subnormal scores keep their order: above +-0, below the smallest
+    normal number, negative ones below -0 (brute force over random rows)."""
+    vals = np.array([-1e-40, -0.0, 0.0, 1e-45, 1e-40, 2e-40, 1.2e-38, -np.inf, np.nan], np.float32)
+    assert vals[3] > 0 and vals[4] < np.finfo(np.float32).tiny            # really subnormal
+    row = np.array([0.0, 1e-45, -1e-40, 2e-40, -0.0], np.float32)
+    assert oracle.topk_indices(row[None, :], 2)[0].tolist() == [1, 3]
+    rng = np.random.default_rng(23)
+    for trial in range(30):
+        L, k = int(rng.integers(1, 40)), int(rng.integers(1, 15))
+        row = vals[rng.integers(0, len(vals), L)]
+        got = oracle.topk_indices(row[None, :], k, offset=3)[0].tolist()
+        assert got == _topk_brute([float(x) for x in row], k, 3), (trial, row, k)
+
+
 # ------------------------------------------------------------------ fp4 compressed rows
 
 def test_e2m1_codes_and_nibble_order():
