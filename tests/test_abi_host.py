@@ -123,8 +123,13 @@ def test_topk_argument_checks(lib):
     assert call(out=2) == INVALID                 # 4-byte alignment
     assert call(offset=-1) == INVALID
     assert call(L=-1) == INVALID
+    assert call(scores=2) == INVALID              # 4-byte alignment of the scores
+    assert call(L=100, stride=100, offset=2**31 - 100) == INVALID   # last position + offset past int32
+    assert call(rows=2**31) == INVALID            # more rows than a grid holds
+    assert call(k=-1) == INVALID
     assert call(rows=0) == OK                     # nothing to do, nothing touched
     assert call(k=0) == OK
+    assert call(rows=0, scores=None, out=None) == OK
 
 
 def test_workspace_size_queries(lib):
