@@ -127,12 +127,19 @@ def _stream_ptr(stream) -> int:
 _ws_cache: dict = {}
 
 
-def _workspace(nbytes: int, device: torch.device, key: str) -> torch.Tensor:
-    """A zero-initialised per-device scratch buffer, grown on demand."""
-    k = (device.index, key)
+def _workspace(nbytes: int, device: torch.device, key: str, stream=None) -> torch.Tensor:
+    """A zero-initialised scratch buffer per device, stream and kind of call,
+    grown on demand.  Calls on different streams get different buffers: the
+    fused calls keep the attention output there between their kernels, so a
+    shared buffer would let concurrent calls overwrite each other's.  Each
+    buffer is allocated on the stream that uses it, so the caching allocator
+    reuses a replaced one only after that stream's pending work."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    k = (device.index, key, int(s.cuda_stream))
     ws = _ws_cache.get(k)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        with torch.cuda.stream(s):
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _ws_cache[k] = ws
     return ws
 
@@ -185,7 +192,7 @@ def sparse_attn(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor, idx: torc
     lib = library()
     need = int(lib.sa_sparse_attn_workspace_size(B, T, H, D, K))
     if workspace is None:
-        workspace = _workspace(need, q.device, "attn")
+        workspace = _workspace(need, q.device, "attn", stream)
     code = lib.sa_sparse_attn(q.data_ptr(), kv.data_ptr(), sink.data_ptr(), idx.data_ptr(),
                               float(scale), B, T, H, D, N, K, out.data_ptr(),
                               1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
@@ -251,7 +258,7 @@ def sparse_attn_two_source(q: torch.Tensor, window_kv: torch.Tensor | None,
     lib = library()
     need = int(lib.sa_sparse_attn_workspace_size(B, T, H, D, K))
     if workspace is None:
-        workspace = _workspace(need, q.device, "attn")
+        workspace = _workspace(need, q.device, "attn", stream)
     code = lib.sa_sparse_attn_two_source(q.data_ptr(), pw, W, sw, pc, C, sc, sink.data_ptr(),
                                          idx.data_ptr(), float(scale), B, T, H, D, K, out.data_ptr(),
                                          1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
@@ -310,7 +317,7 @@ def sparse_attn_two_source_fp4(q: torch.Tensor, window_kv: torch.Tensor | None,
     lib = library()
     need = int(lib.sa_sparse_attn_workspace_size(B, T, H, D, K))
     if workspace is None:
-        workspace = _workspace(need, q.device, "attn")
+        workspace = _workspace(need, q.device, "attn", stream)
     code = lib.sa_sparse_attn_two_source_fp4(q.data_ptr(), pw, W, sw, pc, ps, C, sc, sink.data_ptr(),
                                              idx.data_ptr(), float(scale), B, T, H, D, K, out.data_ptr(),
                                              1 if out.dtype == torch.float32 else 0, workspace.data_ptr(),
@@ -347,7 +354,7 @@ def sparse_attn_rope_wo_a(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor,
     lib = library()
     need = int(lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, H, D, K, G, R))
     if workspace is None:
-        workspace = _workspace(need, q.device, "fused")
+        workspace = _workspace(need, q.device, "fused", stream)
     code = lib.sa_sparse_attn_rope_wo_a(q.data_ptr(), kv.data_ptr(), sink.data_ptr(),
                                         idx.data_ptr(), float(scale), B, T, H, D, N, K,
                                         rope_cos_sin.data_ptr(), rope_dim, wo_a.data_ptr(), G, R,
@@ -388,7 +395,7 @@ def sparse_attn_rope_wo_a_fp8(q: torch.Tensor, kv: torch.Tensor, sink: torch.Ten
     lib = library()
     if workspace is None:
         need = int(lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, H, D, K, G, R))
-        workspace = _workspace(need, q.device, "fused_fp8")
+        workspace = _workspace(need, q.device, "fused_fp8", stream)
     code = lib.sa_sparse_attn_rope_wo_a_fp8(q.data_ptr(), kv.data_ptr(), sink.data_ptr(),
                                             idx.data_ptr(), float(scale), B, T, H, D, N, K,
                                             rope_cos_sin.data_ptr(), rope_dim, wo_a_e4m3.data_ptr(),
@@ -432,7 +439,7 @@ def sparse_attn_block_tail(q: torch.Tensor, kv: torch.Tensor, sink: torch.Tensor
     lib = library()
     need = int(lib.sa_sparse_attn_block_tail_workspace_size(B, T, H, D, K, G, R))
     if workspace is None:
-        workspace = _workspace(need, q.device, "tail")
+        workspace = _workspace(need, q.device, "tail", stream)
     code = lib.sa_sparse_attn_block_tail(q.data_ptr(), kv.data_ptr(), sink.data_ptr(), idx.data_ptr(),
                                          float(scale), B, T, H, D, N, K, rope_cos_sin.data_ptr(),
                                          rope_dim, wo_a.data_ptr(), G, R, wo_b.data_ptr(), dim,

@@ -60,3 +60,9 @@ def oracle_rows(x, queries, scale):
         assert bad == 0
         out[np.searchsorted(queries, sel)] = ref[0]
     return out
+
+
+def cached_workspace(kind: str):
+    """The binding's default workspace of one kind of call ("attn", "fused", ...)
+    on the current device and stream."""
+    return sa._ws_cache[(torch.cuda.current_device(), kind, int(torch.cuda.current_stream().cuda_stream))]

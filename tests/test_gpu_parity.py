@@ -10,7 +10,7 @@ import oracle
 import sparse_latent_attention_02_gb300 as sa
 from sparse_latent_attention_02_gb300 import inputs as I
 
-from parity_util import compare, oracle_rows, sample_queries, to_dev
+from parity_util import cached_workspace, compare, oracle_rows, sample_queries, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def _built():
 def run(x, scale, out_dtype=torch.bfloat16):
     g = to_dev(x)
     out = sa.sparse_attn(g["q"], g["kv"], g["sink"], g["idx"], scale, out_dtype=out_dtype)
-    ws = sa._ws_cache[(torch.cuda.current_device(), "attn")]
+    ws = cached_workspace("attn")
     sa.check_errors(ws)
     return out
 
@@ -82,7 +82,7 @@ def test_fused_tail_workload_sampled():
     x = I.make_inputs(wl, seed=4, device="cuda")
     rope = sa.rope_table(wl.theta, 0, wl.T, wl.rope_dim).cuda()
     y = sa.sparse_attn_rope_wo_a(x["q"], x["kv"], x["sink"], x["idx"], wl.scale, rope, x["wo_a"])
-    sa.check_errors(sa._ws_cache[(torch.cuda.current_device(), "fused")])
+    sa.check_errors(cached_workspace("fused"))
     qs = sample_queries(wl.n_queries, 24, seed=4, include=(0, 5, 4095, 4096, 8191))
     o = oracle_rows(x, qs, wl.scale)
     o = oracle.inverse_rope(o, qs % wl.T, wl.rope_dim, wl.theta)
@@ -170,12 +170,12 @@ def test_bad_index_reported_and_skipped():
     out = sa.sparse_attn(gd["q"], gd["kv"], gd["sink"], gd["idx"], 512 ** -0.5,
                          out_dtype=torch.float32)
     with pytest.raises(sa.SAError) as e:
-        sa.check_errors(sa._ws_cache[(torch.cuda.current_device(), "attn")])
+        sa.check_errors(cached_workspace("attn"))
     assert e.value.code == 4
     ref = full_oracle(dict(q=q, kv=kv, sink=sink, idx=clean), 512 ** -0.5)
     compare(out.double().cpu().numpy(), ref, "bad index skipped")
     # the error word was cleared by the read
-    sa.check_errors(sa._ws_cache[(torch.cuda.current_device(), "attn")])
+    sa.check_errors(cached_workspace("attn"))
 
 
 @pytest.mark.parametrize("mode", ["sink_minus_inf", "dominant_sink", "wide_logits"])
@@ -248,7 +248,7 @@ def test_kv_in_pinned_host_memory():
         sa.sparse_attn(gd["q"], pageable, gd["sink"], gd["idx"], 0.1)
     lib = sa.library()
     out = torch.empty(1, T, 64, 512, dtype=torch.float32, device="cuda")
-    ws = sa._ws_cache[(torch.cuda.current_device(), "attn")]
+    ws = cached_workspace("attn")
     code = lib.sa_sparse_attn(gd["q"].data_ptr(), pageable.data_ptr(), gd["sink"].data_ptr(),
                               gd["idx"].data_ptr(), 0.1, 1, T, 64, 512, N, K, out.data_ptr(), 1,
                               ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
@@ -467,6 +467,38 @@ def test_fused_tail_fp8_matches_dequantized_weight(B, T, K, N, G, R):
     yref = oracle.wo_a(o.reshape(len(qs), G, -1), wdq)
     compare(got.reshape(-1, G * R)[torch.as_tensor(qs, device="cuda")].double().cpu().numpy(),
             yref.reshape(len(qs), -1), f"fp8 tail G{G}")
+
+
+def test_fused_calls_on_two_streams_keep_their_own_workspace():
+    """Fused calls in flight on two streams at once, each with the binding's
+    default workspace (where the attention output waits for the GEMM), give
+    exactly what each gives alone."""
+    g = torch.Generator().manual_seed(5)
+    B, T, K, N, G, R = 2, 300, 192, 400, 8, 512
+
+    def make():
+        q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16)
+        kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16)
+        sink = torch.randn(64, generator=g)
+        idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
+        return to_dev(dict(q=q, kv=kv, sink=sink, idx=idx))
+
+    xs = [make(), make()]
+    w = (0.02 * torch.randn(G, R, 64 * 512 // G, generator=g)).to(torch.bfloat16).cuda()
+    rope = sa.rope_table(160000.0, 0, T, 64).cuda()
+    call = lambda x, st=None: sa.sparse_attn_rope_wo_a(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5,
+                                                       rope, w, stream=st)
+    ref = [call(x) for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(4):
+        for x, st in zip(xs, streams):
+            with torch.cuda.stream(st):
+                outs.append(call(x, st))
+    torch.cuda.synchronize()
+    for i, y in enumerate(outs):
+        assert torch.equal(y, ref[i % 2])
 
 
 def test_fused_tail_fp8_workload_sampled():
