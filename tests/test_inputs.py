@@ -96,3 +96,35 @@ def test_prefill_recipe():
     # valid pairs of the full 8192-query prefill: sum of window + compressed counts
     t = np.arange(8192)
     assert int((np.minimum(t + 1, 128) + np.minimum(512, t // 2)).sum()) == 4972096
+
+
+def test_fused_tail_recipe():
+    """Two batch rows of the prefill recipe at T = 4096: 4,701,312 valid pairs
+    (2 x (516,160 window + 1,834,496 compressed)), compressed rows <= t//2."""
+    wl = I.WORKLOADS["fused_tail"]
+    g = torch.Generator().manual_seed(4)
+    idx = I.make_indices(wl, g).numpy()
+    assert idx.shape == (2, 4096, 640)
+    assert int((idx >= 0).sum()) == 4_701_312
+    t = np.arange(4096)
+    assert int(np.minimum(t + 1, 128).sum()) == 516_160 and int(np.minimum(512, t // 2).sum()) == 1_834_496
+    for b in range(2):
+        for t in [0, 3, 127, 128, 1023, 1024, 2047, 4095]:
+            row = idx[b, t]
+            nw = _check_window(row, t, wl.W)
+            nc = min(512, t // 2)
+            comp = row[nw:nw + nc]
+            assert len(set(comp.tolist())) == nc
+            if nc:
+                assert comp.min() >= wl.W and comp.max() <= wl.W + t // 2
+            assert np.all(row[nw + nc:] == -1)
+    # the two batch rows draw their compressed rows independently
+    assert not np.array_equal(idx[0, 4095], idx[1, 4095])
+
+
+def test_block_tail_shares_the_fused_tail_lists():
+    a, b = I.WORKLOADS["fused_tail"], I.WORKLOADS["block_tail"]
+    assert (a.B, a.T, a.K, a.W, a.C) == (b.B, b.T, b.K, b.W, b.C)
+    ia = I.make_indices(a, torch.Generator().manual_seed(9)).numpy()
+    ib = I.make_indices(b, torch.Generator().manual_seed(9)).numpy()
+    assert np.array_equal(ia, ib)
