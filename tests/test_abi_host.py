@@ -34,6 +34,47 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(sa.EXPORTS)
 
 
+def _declarations():
+    """name -> (return type, [parameter types]) of every function in sa.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for ret, name, params in re.findall(r"(sa_status|size_t|const char \*)\s*(sa_[a-z0-9_]+)\s*\(([^)]*)\)\s*;",
+                                         text):
+        types = [re.sub(r"\s+[A-Za-z_][A-Za-z0-9_]*$", "", x.strip()) for x in params.split(",")]
+        out[name] = (ret, [t for t in types if t and t != "void"])
+    return out
+
+
+def _kind(c_type):
+    """The C type of a header parameter as the ctypes type the binding must use."""
+    if "*" in c_type:
+        return "pointer"
+    return {"int": "int", "sa_dtype": "int", "sa_status": "int", "int64_t": "int64", "size_t": "size",
+            "float": "float", "double": "double"}[c_type]
+
+
+def _ctypes_kind(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "pointer"
+    return {ctypes.c_int: "int", ctypes.c_int64: "int64", ctypes.c_size_t: "size", ctypes.c_float: "float",
+            ctypes.c_double: "double"}[t]
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every function's ctypes argument list has the header's arity and, slot
+    by slot, its kind (pointer, int, int64, size_t, float, double); return
+    types too.  A slip here would pass garbage through the ABI unseen."""
+    decl = _declarations()
+    assert set(decl) == set(sa.EXPORTS)
+    for name, (ret, params) in decl.items():
+        fn = getattr(lib, name)
+        got = [_ctypes_kind(t) for t in fn.argtypes]
+        assert got == [_kind(p) for p in params], name
+        want_ret = {"sa_status": ctypes.c_int, "size_t": ctypes.c_size_t, "const char *": ctypes.c_char_p}[ret]
+        assert fn.restype == want_ret, name
+
+
 def test_status_strings(lib):
     for code in range(7):
         s = lib.sa_status_string(code).decode()
