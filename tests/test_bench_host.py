@@ -70,3 +70,31 @@ def test_launch_counts_per_call():
     assert bench.launches_per_call(I.WORKLOADS["decode"], 148) == 1
     assert bench.launches_per_call(I.WORKLOADS["fused_tail"], 148) == 2
     assert bench.launches_per_call(I.WORKLOADS["block_tail"], 148) == 3
+
+
+def _bench(env_extra, *args):
+    import json
+    import subprocess
+    env = dict(os.environ, OMP_NUM_THREADS="4", **env_extra)
+    p = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), *args], cwd=bench.ROOT, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [json.loads(x) for x in p.stdout.splitlines() if x.startswith("{")]
+    return lines
+
+
+def test_reference_arm_prints_one_line_on_rank_zero_only():
+    """The oracle arm: one JSON line from rank 0 with the contract's keys, on
+    the headline workload; any other rank of a launch exits at once, silent."""
+    ranks = dict(WORLD_SIZE="2", MASTER_ADDR="127.0.0.1", MASTER_PORT="29599")
+    args = ("--impl", "reference", "--steps", "1", "--warmup", "1")
+    assert _bench(dict(ranks, RANK="1", LOCAL_RANK="1"), *args) == []
+    (line,) = _bench(dict(ranks, RANK="0", LOCAL_RANK="0"), *args)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["unit"] == "queries/s" and line["value"] > 0
+    assert line["steps"] == 1 and line["warmup"] == 3          # raised to the minimum of three
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["workload"].startswith("decode: B=64 T=1")
