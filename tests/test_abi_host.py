@@ -239,3 +239,51 @@ def test_fp8_tail_workspace_size(lib):
         base = lib.sa_sparse_attn_rope_wo_a_workspace_size(B, T, 64, 512, 640, 8, 1024)
         got = lib.sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, 64, 512, 640, 8, 1024)
         assert got == base + 1024 * 64 * 512 * 2 and got % 256 == 0
+
+
+class _Schedule(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int), ("split", ctypes.c_int), ("per_cta", ctypes.c_int64),
+                ("pieces", ctypes.c_int)]
+
+
+def _schedule_fn(lib):
+    # sa::attn_schedule(int64_t BT, int K, int num_sms): host arithmetic only
+    fn = getattr(lib, "_ZN2sa13attn_scheduleElii")
+    fn.restype = _Schedule
+    fn.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    return fn
+
+
+def test_attention_schedule_on_the_workload_shapes(lib):
+    sched = _schedule_fn(lib)
+    s = sched(64, 640, 152)          # decode: two pieces of 320 entries, one wave of 128 CTAs
+    assert (s.split, s.pieces, s.per_cta, s.grid) == (1, 2, 320, 128)
+    s = sched(128, 640, 152)         # long decode: whole queries, one CTA each
+    assert (s.split, s.pieces, s.grid) == (0, 1, 128)
+    s = sched(8192, 640, 152)        # prefill: a persistent grid of one CTA per SM
+    assert (s.split, s.pieces, s.grid) == (0, 1, 152)
+    s = sched(16, 192, 152)          # tiny: two pieces (the list holds two 128-row chunks at most)
+    assert (s.split, s.pieces, s.per_cta, s.grid) == (1, 2, 96, 32)
+    s = sched(1, 1024, 152)          # one query, the longest list: the cluster limit
+    assert (s.pieces, s.per_cta, s.grid) == (8, 128, 8)
+
+
+def test_attention_schedule_invariants(lib):
+    """For any shape: one wave of CTAs; pieces a power of two within the
+    cluster limit and no more than the list's 128-row chunks; pieces a
+    multiple of 32 entries that cover the list, none of them empty."""
+    sched = _schedule_fn(lib)
+    rng = np.random.default_rng(8)
+    for _ in range(3000):
+        sms = int(rng.integers(1, 200))
+        BT = int(rng.integers(1, 3 * sms))
+        K = int(rng.integers(1, 1025))
+        s = sched(BT, K, sms)
+        if s.split == 0:
+            assert s.pieces == 1 and s.grid == min(BT, sms)
+            continue
+        P = s.pieces
+        assert P >= 2 and P & (P - 1) == 0 and P <= 8 and P <= -(-K // 128)
+        assert s.grid == BT * P <= sms
+        assert s.per_cta % 32 == 0 and P * s.per_cta >= K and (P - 1) * s.per_cta < K
+    assert sched(0, 640, 152).grid == 0 and sched(5, 0, 152).split == 0
