@@ -3,9 +3,12 @@
 Default (our arm): the decode workload (B=64 queries, 640-entry index lists,
 8192-token context at ratio 2 -> 4224 latent rows per batch row), timed as one
 `sa_sparse_attn` call per step over rotating input sets whose total size
-exceeds L2, replayed from a CUDA graph.  Prints ONE JSON line.  The prefill,
-long-context decode and fused-tail workloads are measured too and reported
-under "workloads".
+exceeds L2, replayed from a CUDA graph.  Prints ONE JSON line.  The other
+lines are measured too and reported under "workloads": long-context decode,
+prefill, the fused tail (attention, inverse RoPE, grouped wo_a), the block
+tail (plus wo_b), decode with fp4 compressed rows, the fused tail with an
+fp8 wo_a, and the top-k selection (8192 rows x 4096 scores -> 512).
+--extra NAME times one of them alone.
 
 --impl reference: the fp64 CPU oracle, timed as it stands on the host cores
 on a bounded sample of the same workload (the only reference this path has).
