@@ -275,11 +275,13 @@ sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim,
  * cudaFree, no allocating library routine.
  *
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
- * contents: each call zeroes its error word (enqueued on `stream` before the
- * kernels), so calls whose work overlaps on the GPU race and must not be
- * issued on different streams at the same time.
+ * device current) and caches it for the life of the process; make that first
+ * call before any stream capture.  The cached address does not survive
+ * cudaDeviceReset on that device.  All calls share the one array and it keeps
+ * the last call's contents: each call zeroes its error word (enqueued on
+ * `stream` after every host check has passed, right before the kernel), so
+ * calls whose work overlaps on the GPU race and must not be issued on
+ * different streams at the same time.
  *
  * Arguments as for sa_sparse_attn, without workspace/ws_bytes.  If scratch_out
  * is not NULL it receives the array's device address; pass it to

@@ -4,6 +4,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <mutex>
 
 #include "sa_internal.h"
@@ -27,6 +28,21 @@ uint64_t wait_timeout_ns()
         return (uint64_t)ms * 1000000ull;
     }();
     return ns;
+}
+
+// Test hook for failure detection, read once per process: SA_TEST_HOLD_LISTS=n
+// makes the first n attention calls of the process withhold their first
+// index list, so their bounded waits run out and they report SA_ERR_TIMEOUT
+// without faulting or hanging the GPU; later calls run normally.
+bool hold_lists()
+{
+    static const long holds = [] {
+        const char *e = std::getenv("SA_TEST_HOLD_LISTS");
+        const long n = e ? std::strtol(e, nullptr, 10) : 0;
+        return n > 0 ? n : 0L;
+    }();
+    static std::atomic<long> calls{0};
+    return holds > 0 && calls.fetch_add(1) < holds;
 }
 
 bool current_sms(int *sms)
@@ -134,11 +150,7 @@ sa_status fill_attn_params(AttnParams &p, const void *q, const KvSources &src, c
     p.K = K;
     p.out_f32 = out_f32 ? 1 : 0;
     p.timeout_ns = wait_timeout_ns();
-    // Test hook for failure detection: SA_TEST_HOLD_LISTS=1 makes the kernel
-    // withhold its first index list, so its bounded waits run out and the call
-    // reports SA_ERR_TIMEOUT without faulting or hanging the GPU.
-    const char *hold = std::getenv("SA_TEST_HOLD_LISTS");
-    p.hold_lists = (hold && hold[0] == '1') ? 1 : 0;
+    p.hold_lists = hold_lists() ? 1 : 0;
     return SA_OK;
 }
 
@@ -199,6 +211,40 @@ sa_status check_attn_args(const void *q, const void *kv, const float *sink, cons
     return SA_OK;
 }
 
+sa_status attn_call(const void *q, const void *kv, const float *sink, const int32_t *idx, float scale, int B,
+                    int T, int H, int D, int N, int K, void *out, sa_dtype out_dtype, void *workspace,
+                    size_t ws_bytes, cudaStream_t s, bool clear_error_word)
+{
+    sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
+    if (st != SA_OK)
+        return st;
+    if (out_dtype != SA_BF16 && out_dtype != SA_F32)
+        return SA_ERR_INVALID_ARG;
+    const int64_t BT = (int64_t)B * T;
+    if (BT == 0)
+        return SA_OK;
+    if (ws_bytes < attn_workspace_bytes(BT, K))
+        return SA_ERR_WORKSPACE;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
+    const size_t esz = out_dtype == SA_F32 ? 4 : 2;
+    AttnParams p;
+    if (K > 0) {
+        const KvSources src{kv, N, N, nullptr, 0};
+        st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
+        if (st != SA_OK)
+            return st;
+    }
+    // every host check has passed: from here on only enqueueing
+    if (clear_error_word && cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess)
+        return SA_ERR_CUDA;
+    if (K == 0)
+        return cudaMemsetAsync(out, 0, (size_t)BT * H * D * esz, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+    const Schedule sch = attn_schedule(BT, K, sms);
+    return launch_attention(p, sch, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+}
+
 namespace {
 
 // The driver's cuTensorMapEncodeTiled, looked up once (null if unavailable).
@@ -257,42 +303,17 @@ size_t sa_sparse_attn_workspace_size(int B, int T, int H, int D, int K)
 {
     (void)H;
     (void)D;
-    int sms = 0;
-    if (!current_sms(&sms))
-        sms = 1;
     if (B < 0 || T < 0 || K < 0)
         return WS_HEADER;
-    return attn_workspace_bytes((int64_t)B * T, K, sms);
+    return attn_workspace_bytes((int64_t)B * T, K);
 }
 
 sa_status sa_sparse_attn(const void *q, const void *kv, const float *sink, const int32_t *idx,
                          float scale, int B, int T, int H, int D, int N, int K, void *out,
                          sa_dtype out_dtype, void *workspace, size_t ws_bytes, void *stream)
 {
-    sa_status st = check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out, workspace);
-    if (st != SA_OK)
-        return st;
-    if (out_dtype != SA_BF16 && out_dtype != SA_F32)
-        return SA_ERR_INVALID_ARG;
-    const int64_t BT = (int64_t)B * T;
-    if (BT == 0)
-        return SA_OK;
-    int sms = 0;
-    if (!current_sms(&sms))
-        return SA_ERR_CUDA;
-    if (ws_bytes < attn_workspace_bytes(BT, K, sms))
-        return SA_ERR_WORKSPACE;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t esz = out_dtype == SA_F32 ? 4 : 2;
-    if (K == 0)
-        return cudaMemsetAsync(out, 0, (size_t)BT * H * D * esz, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
-    AttnParams p;
-    const KvSources src{kv, N, N, nullptr, 0};
-    st = fill_attn_params(p, q, src, sink, idx, scale, B, T, N, K, out, out_dtype == SA_F32, workspace);
-    if (st != SA_OK)
-        return st;
-    const Schedule sch = attn_schedule(BT, K, sms);
-    return launch_attention(p, sch, s) == cudaSuccess ? SA_OK : SA_ERR_CUDA;
+    return attn_call(q, kv, sink, idx, scale, B, T, H, D, N, K, out, out_dtype, workspace, ws_bytes,
+                     static_cast<cudaStream_t>(stream), false);
 }
 
 // Shared by the two-source entry points: checks, then one launch.
@@ -326,11 +347,11 @@ static sa_status two_source_call(const void *q, const KvSources &src, int C, con
             (int64_t)B * (C > 0 ? src.kv2_bstride : 0) >= ((int64_t)1 << 40))
             return SA_ERR_UNSUPPORTED;
     }
+    if (ws_bytes < attn_workspace_bytes(BT, K))
+        return SA_ERR_WORKSPACE;
     int sms = 0;
     if (!current_sms(&sms))
         return SA_ERR_CUDA;
-    if (ws_bytes < attn_workspace_bytes(BT, K, sms))
-        return SA_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t esz = out_dtype == SA_F32 ? 4 : 2;
     if (K == 0)
@@ -456,13 +477,13 @@ sa_status sa_sparse_attn_rope_wo_a(const void *q, const void *kv, const float *s
         return st;
     if (BT >= ((int64_t)1 << 31) / 128)
         return SA_ERR_UNSUPPORTED;
-    int sms = 0;
-    if (!current_sms(&sms))
-        return SA_ERR_CUDA;
-    const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
+    const size_t attn_ws = round256(attn_workspace_bytes(BT, K));
     const size_t o_bytes = round256((size_t)BT * H * D * 2);
     if (ws_bytes < attn_ws + o_bytes)
         return SA_ERR_WORKSPACE;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
     return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, nullptr, G, R,
                           out, workspace, attn_ws, sms, static_cast<cudaStream_t>(stream));
 }
@@ -484,15 +505,15 @@ sa_status sa_sparse_attn_rope_wo_a_fp8(const void *q, const void *kv, const floa
         return st;
     if (BT >= ((int64_t)1 << 31) / 128)
         return SA_ERR_UNSUPPORTED;
-    int sms = 0;
-    if (!current_sms(&sms))
-        return SA_ERR_CUDA;
-    const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
+    const size_t attn_ws = round256(attn_workspace_bytes(BT, K));
     const size_t o_bytes = round256((size_t)BT * H * D * 2);
     const bool decode_first = BT >= FP8_DECODE_FIRST_TOKENS;
     const size_t w_bytes = decode_first ? round256((size_t)R * H * D * 2) : 0;   // bf16 copy of wo_a
     if (ws_bytes < attn_ws + o_bytes + w_bytes)
         return SA_ERR_WORKSPACE;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!decode_first)   // few tokens: the GEMM decodes the weight blocks itself
         return attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a_e4m3,
@@ -545,14 +566,14 @@ sa_status sa_sparse_attn_block_tail(const void *q, const void *kv, const float *
         return SA_ERR_INVALID_ARG;
     if (BT >= ((int64_t)1 << 31) / 128)
         return SA_ERR_UNSUPPORTED;
-    int sms = 0;
-    if (!current_sms(&sms))
-        return SA_ERR_CUDA;
-    const size_t attn_ws = round256(attn_workspace_bytes(BT, K, sms));
+    const size_t attn_ws = round256(attn_workspace_bytes(BT, K));
     const size_t o_bytes = round256((size_t)BT * H * D * 2);
     const size_t y_bytes = round256((size_t)BT * G * R * 2);
     if (ws_bytes < attn_ws + o_bytes + y_bytes)
         return SA_ERR_WORKSPACE;
+    int sms = 0;
+    if (!current_sms(&sms))
+        return SA_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *y = static_cast<uint8_t *>(workspace) + attn_ws + o_bytes;
     st = attn_rope_wo_a(q, kv, sink, idx, scale, B, T, H, D, N, K, rope_cos_sin, rope_dim, wo_a, nullptr, G, R,

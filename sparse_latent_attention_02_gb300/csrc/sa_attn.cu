@@ -90,9 +90,9 @@ constexpr uint32_t OFF_SEGN = OFF_AUX + 64 * 4;        // int [2] list lengths
 constexpr uint32_t OFF_BAR = OFF_SEGN + 16;            // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;        // [0] TMEM base, [1] abort flag
 constexpr uint32_t OFF_RAW = OFF_MISC + 64;           // int32 [SA_MAX_K] list as read from idx
-constexpr uint32_t OFF_XSTAT = OFF_RAW + 4 * SA_MAX_K;   // float [pieces][2][64 / pieces] peers' (m, l)
-constexpr uint32_t OFF_XSEND = OFF_XSTAT + 2 * 64 * 4;   // float [2][64 / pieces] (m, l) being sent
-constexpr uint32_t OFF_SINK = OFF_XSEND + 2 * 64 * 4;    // float [64] sink * log2(e)
+constexpr uint32_t OFF_XSTAT = OFF_RAW + 4 * SA_MAX_K;   // float [pieces][3][64 / pieces] peers' (m, l, k)
+constexpr uint32_t OFF_XSEND = OFF_XSTAT + 3 * 64 * 4;   // float [3][64 / pieces] (m, l, k) being sent
+constexpr uint32_t OFF_SINK = OFF_XSEND + 3 * 64 * 4;    // float [64] sink * log2(e)
 constexpr uint32_t SMEM_USED = OFF_SINK + 64 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -687,26 +687,35 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 
 // Split schedule: the P pieces of one query's list run as one cluster, and
 // CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  Every
-// CTA sends each peer its unnormalised O^T columns (scaled by row_scale(l),
-// as fp16 pairs of adjacent heads) and its (m, l) for that peer's heads into
-// the peer's chunk buffer: it stages them in its own slot
-// of its own chunk buffer (the slot no peer writes) and moves them with one
-// bulk shared-to-shared copy per peer, which completes on the peer's XFULL
-// barrier.  A CTA offers its buffer (arrives on each peer's XRDY barrier)
-// once its own last PV product is done.  The receiver merges the pieces:
+// CTA sends each peer its unnormalised O^T columns for that peer's heads, as
+// fp16 pairs of adjacent heads after an exact per-head power-of-two scaling
+// 2^k (k = head_exponent of the head's largest |O| in this piece), together
+// with its (m, l, k) for those heads, into the peer's chunk buffer: it stages
+// them in its own slot of its own chunk buffer (the slot no peer writes) and
+// moves them with one bulk shared-to-shared copy per peer, which completes on
+// the peer's XFULL barrier.  A CTA offers its buffer (arrives on each peer's
+// XRDY barrier) once its own last PV product is done.  The receiver merges
+// the pieces:
 //   M = max_r m_r (each m_r starts at the sink),  w_r = 2^(m_r - M),
-//   o = sum_r w_r O_r / (sum_r w_r l_r + 2^(sink*log2e - M))
+//   o = sum_r w_r 2^-k_r (2^k_r O_r) / (sum_r w_r l_r + 2^(sink*log2e - M))
 // then applies the inverse RoPE when asked and writes its heads.  Softmax
 // warps only: warp (quarter qd, half hf) handles features 128d + 32qd + lane
 // of tiles d = 2hf, 2hf + 1.  False when a wait ran out.
-// 2^-e for a row sum l = f * 2^e, f in [0.5, 1) (0 for l = 0): scaling a
-// piece's O by it is exact and leaves every entry within the largest |value|
-// of the rows it sums (|O| <= l * max|v| and 2^-e <= 1 / l).
-__device__ __forceinline__ float row_scale(float l)
+//
+// Exponent of the scaling that brings a head's largest |O| = f * 2^e, f in
+// [0.5, 1), to f * 2^15, inside fp16's range (65504) with its full 11-bit
+// precision, whatever the magnitude of kv or of the row sum: k = 15 - e,
+// capped at 127 so that 2^k stays a finite float (a head whose largest
+// entry is below 2^-112 keeps less precision, at a magnitude that cannot
+// matter).  0 for an all-zero head (or a non-finite one).  The scaling is
+// exact, so integer-valued partials (the index-probe case) stay exact.
+__device__ __forceinline__ int head_exponent(float max_abs)
 {
+    if (!(max_abs > 0.f) || !(max_abs <= 3.402823466e38f))
+        return 0;
     int e;
-    (void)frexpf(l, &e);
-    return l > 0.f ? ldexpf(1.f, -e) : 0.f;
+    (void)frexpf(max_abs, &e);
+    return min(15 - e, 127);
 }
 
 template <int P>
@@ -715,10 +724,10 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
 {
     constexpr int HP = H / P;
     // one piece's O for HP heads, [HP][512], sent as fp16 after an exact
-    // power-of-two scaling by row_scale(l) (bounded then by the largest |value|
-    // of the rows; integers and their halvings stay exact)
+    // per-head power-of-two scaling (largest |entry| in [2^14, 2^15))
     constexpr uint32_t SLOT_BYTES = HP * D * 2;
-    constexpr uint32_t STAT_BYTES = 2 * HP * 4;      // its (m, l) for HP heads
+    constexpr uint32_t STAT_BYTES = 3 * HP * 4;      // its (m, l, k) for HP heads
+    static_assert(STAT_BYTES % 16 == 0, "bulk copy size");
     constexpr int COPY_PARTS = 8;                    // a slot goes as 8 copies issued by 8 threads
     const uint32_t me = cluster_ctarank();
     const uint32_t bar0 = sbase + OFF_BAR;
@@ -726,7 +735,10 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     const float *lt = reinterpret_cast<const float *>(smem + OFF_AUX);   // this piece's row sums
     const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);
     float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights, then [HP] 1/den
-    float *inv_l = wts;                                       // [64] row_scale(l) while sending
+    // in the P buffer (free once the last PV is done) while sending:
+    float *xmax = reinterpret_cast<float *>(smem + OFF_P);    // [8 warps][64] largest |O| per head
+    float *hscale = xmax + NUM_SOFTMAX_WARPS * 64;            // [64] 2^k
+    float *hexp = hscale + 64;                                // [64] k
     // [P][HP / 2][512] pairs of heads (2j, 2j + 1) per feature
     const __half2 *recv = reinterpret_cast<const __half2 *>(smem + OFF_KV);
     __half2 *stage = reinterpret_cast<__half2 *>(smem + OFF_KV + me * SLOT_BYTES);
@@ -737,8 +749,38 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         mbar_arrive_expect_tx(bar0 + 8 * B_XFULL, (P - 1) * (SLOT_BYTES + STAT_BYTES));
     if (t < P && t != (int)me)
         mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
-    if (t < H)
-        inv_l[t] = row_scale(lt[t]);
+    // each head's largest |O| over this piece's 512 features: per warp over its
+    // 32 features of two tiles, then over the eight warps
+    const int wi = t >> 5;
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        float mx[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            mx[i] = 0.f;
+        if (nc > 0) {
+#pragma unroll 1
+            for (int e = 0; e < 2; ++e) {
+                uint32_t v[32];
+                tmem_ld32(tl + TM_O + 64 * (2 * hf + e) + 32 * hh, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    mx[i] = fmaxf(mx[i], fabsf(__uint_as_float(v[i])));
+            }
+        }
+        xmax[wi * 64 + 32 * hh + lane] = warp_reduce32<true>(mx, lane);
+    }
+    bar_sync(1, SMX_THREADS);
+    if (t < H) {
+        float mx = 0.f;
+#pragma unroll
+        for (int w = 0; w < NUM_SOFTMAX_WARPS; ++w)
+            mx = fmaxf(mx, xmax[w * 64 + t]);
+        const int k = head_exponent(mx);
+        hscale[t] = ldexpf(1.f, k);
+        hexp[t] = (float)k;
+    }
     bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
     if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
         return false;
@@ -758,6 +800,7 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         if (t < HP) {
             xsend[t] = m_s[g * HP + t];
             xsend[HP + t] = lt[g * HP + t];
+            xsend[2 * HP + t] = hexp[g * HP + t];
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -776,8 +819,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
 #pragma unroll
             for (int i = 0; i < HP; i += 2)
                 stage[(i / 2) * D + 128 * d + fl] =
-                    __floats2half2_rn(__uint_as_float(v[i]) * inv_l[g * HP + i],
-                                      __uint_as_float(v[i + 1]) * inv_l[g * HP + i + 1]);
+                    __floats2half2_rn(__uint_as_float(v[i]) * hscale[g * HP + i],
+                                      __uint_as_float(v[i + 1]) * hscale[g * HP + i + 1]);
         }
         fence_proxy_async_smem();
         bar_sync(1, SMX_THREADS);
@@ -805,15 +848,15 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
 #pragma unroll
         for (int r = 0; r < P; ++r)
             if (r != (int)me)
-                M = fmaxf(M, xst[r * 2 * HP + t]);
+                M = fmaxf(M, xst[r * 3 * HP + t]);
         float den = 0.f;
 #pragma unroll
         for (int r = 0; r < P; ++r) {
-            const float mr = r == (int)me ? m_s[h] : xst[r * 2 * HP + t];
-            const float lr = r == (int)me ? lt[h] : xst[r * 2 * HP + HP + t];
+            const float mr = r == (int)me ? m_s[h] : xst[r * 3 * HP + t];
+            const float lr = r == (int)me ? lt[h] : xst[r * 3 * HP + HP + t];
             const float w = M == -INFINITY ? 0.f : ex2(mr - M);
-            // peers' O arrive multiplied by row_scale(l): undo it exactly
-            wts[r * HP + t] = r == (int)me ? w : (lr > 0.f ? w / row_scale(lr) : 0.f);
+            // peers' O arrive multiplied by 2^k: undo it exactly
+            wts[r * HP + t] = r == (int)me ? w : ldexpf(w, -(int)xst[r * 3 * HP + 2 * HP + t]);
             den += w * lr;
         }
         den += M == -INFINITY ? 0.f : ex2(sl - M);
@@ -1262,10 +1305,11 @@ Schedule attn_schedule(int64_t BT, int K, int num_sms)
     return s;
 }
 
-size_t attn_workspace_bytes(int64_t BT, int K, int num_sms)
+size_t attn_workspace_bytes(int64_t BT, int K)
 {
-    const Schedule s = attn_schedule(BT, K, num_sms);
-    (void)s;
+    (void)BT;
+    (void)K;
+    // the split pieces of a query merge on chip: only the error header
     return WS_HEADER;
 }
 

@@ -57,7 +57,9 @@ struct Schedule {
 
 // Decide the grid and the split of the index lists for this shape and device.
 Schedule attn_schedule(int64_t BT, int K, int num_sms);
-size_t attn_workspace_bytes(int64_t BT, int K, int num_sms);
+// Workspace bytes of the attention call (a function of the shape only, so that
+// a short workspace is refused before any CUDA call).
+size_t attn_workspace_bytes(int64_t BT, int K);
 
 // Enqueue the attention kernel (a cluster launch in the split schedule).
 cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st);
@@ -81,6 +83,14 @@ cudaError_t launch_dequant_fp8(const uint8_t *w8, const float *scales, uint16_t 
 // Top-k selection of positions per row of scores (see sa_topk_indices).
 cudaError_t launch_topk(const float *scores, int64_t row_stride, int64_t rows, int L, int k, int offset,
                         int32_t *out, cudaStream_t st);
+
+// The one-source attention call (sa_sparse_attn) with every host check done
+// before anything is enqueued; with clear_error_word, the workspace's 4-byte
+// error word is zeroed on the stream after the checks, right before the
+// launch (for callers whose scratch keeps an earlier call's contents).
+sa_status attn_call(const void *q, const void *kv, const float *sink, const int32_t *idx, float scale, int B,
+                    int T, int H, int D, int N, int K, void *out, sa_dtype out_dtype, void *workspace,
+                    size_t ws_bytes, cudaStream_t stream, bool clear_error_word);
 
 // Host argument checks of the attention entry points (no CUDA call).
 sa_status check_attn_args(const void *q, const void *kv, const float *sink, const int32_t *idx,

@@ -26,8 +26,10 @@ std::mutex g_mutex;
 void *g_scratch_ptr[MAX_DEVICES] = {};
 
 // Device address of g_scratch on the current device.  Looked up once per
-// device (with that device current); the name g_scratch itself is only a
-// host-side stand-in and must never be handed to a kernel.
+// device (with that device current) and kept for the life of the process;
+// the name g_scratch itself is only a host-side stand-in and must never be
+// handed to a kernel.  The kept address does not survive cudaDeviceReset (or
+// anything else that unloads the library's device code on that device).
 sa_status scratch_address(void **out)
 {
     int dev = 0;
@@ -51,29 +53,26 @@ extern "C" sa_status sa_sparse_attn_noalloc(const void *q, const void *kv, const
                                             int D, int N, int K, void *out, sa_dtype out_dtype,
                                             void **scratch_out, void *stream)
 {
-    // the same host checks as sa_sparse_attn, before anything is enqueued
+    // the host checks that need no device first (a dummy, aligned workspace
+    // address stands in for the scratch array here)
     sa_status st = sa::check_attn_args(q, kv, sink, idx, scale, B, T, H, D, N, K, out,
                                        reinterpret_cast<void *>(256));
     if (st != SA_OK)
         return st;
     if (out_dtype != SA_BF16 && out_dtype != SA_F32)
         return SA_ERR_INVALID_ARG;
+    // Shapes whose scratch would not fit the static array are refused before
+    // anything is enqueued.
+    if ((int64_t)B * T > 0 && sa::attn_workspace_bytes((int64_t)B * T, K) > SCRATCH_BYTES)
+        return SA_ERR_WORKSPACE;
     void *ws = nullptr;
     st = scratch_address(&ws);
     if (st != SA_OK)
         return st;
     if (scratch_out)
         *scratch_out = ws;
-    // Shapes whose scratch would not fit the static array are refused here,
-    // before anything is enqueued.
-    if (sa_sparse_attn_workspace_size(B, T, H, D, K) > SCRATCH_BYTES)
-        return SA_ERR_WORKSPACE;
-    if ((int64_t)B * T == 0)
-        return SA_OK;
-    // The array keeps the previous call's contents: the error word must start
-    // at zero for this call's report.
-    if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return SA_ERR_CUDA;
-    return sa_sparse_attn(q, kv, sink, idx, scale, B, T, H, D, N, K, out, out_dtype, ws,
-                          SCRATCH_BYTES, stream);
+    // The array keeps the previous call's contents: the call clears the error
+    // word on the stream, after all of its host checks, right before its launch.
+    return sa::attn_call(q, kv, sink, idx, scale, B, T, H, D, N, K, out, out_dtype, ws, SCRATCH_BYTES,
+                         static_cast<cudaStream_t>(stream), true);
 }

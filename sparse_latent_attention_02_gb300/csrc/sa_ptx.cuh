@@ -95,7 +95,21 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
     }
 }
 
-// ------------------------------------------------------------------ fences, barriers
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Wait until the grids this one depends on (the previous kernel in the
+// stream, under programmatic dependent launch) have completed and their
+// memory operations are visible; a no-op without that launch attribute.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel in the stream to be scheduled before this grid ends.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // ------------------------------------------------------------------ clusters
 
@@ -182,6 +196,7 @@ __device__ __forceinline__ void bulk_wait_read_all()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+
 // Every thread of every CTA of the cluster (warp-converged).
 __device__ __forceinline__ void cluster_sync()
 {
@@ -255,18 +270,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
-// Four-row gather: rows y0..y3, columns [x, x + box) of a 2-D tensor map whose
-// box is one row high, into four consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
         : "memory");
 }
 

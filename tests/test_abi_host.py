@@ -287,3 +287,35 @@ def test_attention_schedule_invariants(lib):
         assert s.grid == BT * P <= sms
         assert s.per_cta % 32 == 0 and P * s.per_cta >= K and (P - 1) * s.per_cta < K
     assert sched(0, 640, 152).grid == 0 and sched(5, 0, 152).split == 0
+
+
+WORKSPACE = 3
+
+
+def test_workspace_one_byte_short_is_refused(lib):
+    """Every entry point that takes a workspace refuses one a byte smaller
+    than its size query with SA_ERR_WORKSPACE, before any CUDA call (so the
+    check holds without a device; the pointers are never dereferenced)."""
+    L = lib
+    for B, T, K in [(1, 16, 192), (64, 1, 640), (2, 4096, 640), (3, 5, 0)]:
+        need = L.sa_sparse_attn_workspace_size(B, T, 64, 512, K)
+        assert _attn(L, B=B, T=T, K=K, wsb=need - 1) == WORKSPACE
+        assert _attn(L, B=B, T=T, K=K, wsb=need) != WORKSPACE
+        two = lambda wsb: L.sa_sparse_attn_two_source(16, 16, 4, 4, 16, 4, 4, 16, 16, 0.1, B, T, 64, 512, K,
+                                                      16, 0, 256, wsb, None)
+        assert two(need - 1) == WORKSPACE and two(need) != WORKSPACE
+        fp4 = lambda wsb: L.sa_sparse_attn_two_source_fp4(16, 16, 4, 4, 16, 16, 4, 4, 16, 16, 0.1, B, T, 64,
+                                                          512, K, 16, 0, 256, wsb, None)
+        assert fp4(need - 1) == WORKSPACE and fp4(need) != WORKSPACE
+        fneed = L.sa_sparse_attn_rope_wo_a_workspace_size(B, T, 64, 512, K, 8, 1024)
+        fused = lambda wsb: L.sa_sparse_attn_rope_wo_a(16, 16, 16, 16, 0.1, B, T, 64, 512, 8, K, 16, 64, 16,
+                                                       8, 1024, 16, 256, wsb, None)
+        assert fused(fneed - 1) == WORKSPACE and fused(fneed) != WORKSPACE
+        eneed = L.sa_sparse_attn_rope_wo_a_fp8_workspace_size(B, T, 64, 512, K, 8, 1024)
+        fp8 = lambda wsb: L.sa_sparse_attn_rope_wo_a_fp8(16, 16, 16, 16, 0.1, B, T, 64, 512, 8, K, 16, 64,
+                                                         16, 16, 8, 1024, 16, 256, wsb, None)
+        assert fp8(eneed - 1) == WORKSPACE and fp8(eneed) != WORKSPACE
+        bneed = L.sa_sparse_attn_block_tail_workspace_size(B, T, 64, 512, K, 8, 1024)
+        tail = lambda wsb: L.sa_sparse_attn_block_tail(16, 16, 16, 16, 0.1, B, T, 64, 512, 8, K, 16, 64, 16,
+                                                       8, 1024, 16, 5120, 16, 256, wsb, None)
+        assert tail(bneed - 1) == WORKSPACE and tail(bneed) != WORKSPACE

@@ -14,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import sparse_latent_attention_02_gb300 as sa
 from sparse_latent_attention_02_gb300 import inputs as I
 
@@ -22,10 +23,10 @@ from parity_util import compare
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(seed, B, T, K, N, bad=False):
+def _inputs(seed, B, T, K, N, bad=False, kv_scale=1.0):
     g = torch.Generator().manual_seed(seed)
     q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16).cuda()
-    kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16).cuda()
+    kv = (I.rms_rows(torch.randn(B, N, 512, generator=g)) * kv_scale).to(torch.bfloat16).cuda()
     sink = torch.randn(64, generator=g).cuda()
     idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
     idx[torch.rand(B, T, K, generator=g) < 0.1] = -1
@@ -46,15 +47,16 @@ def _noalloc(lib, q, kv, sink, idx, out):
     return code, scratch.value
 
 
-@pytest.mark.parametrize("B,T,K,N,dtype", [
-    (8, 1, 640, 4224, torch.bfloat16),     # few queries: split lists merged inside a cluster
-    (2, 100, 300, 700, torch.float32),     # enough queries for whole lists per CTA
+@pytest.mark.parametrize("B,T,K,N,dtype,kv_scale", [
+    (8, 1, 640, 4224, torch.bfloat16, 1.0),     # few queries: split lists merged inside a cluster
+    (8, 1, 640, 4224, torch.float32, 1e5),      # the same, kv far above fp16's range
+    (2, 100, 300, 700, torch.float32, 1.0),     # enough queries for whole lists per CTA
 ])
-def test_noalloc_matches_workspace_entry_two_calls(B, T, K, N, dtype):
+def test_noalloc_matches_workspace_entry_two_calls(B, T, K, N, dtype, kv_scale):
     sa.build()
     lib = sa.library()
     for call, seed in enumerate((101, 202)):
-        q, kv, sink, idx = _inputs(seed + B, B, T, K, N)
+        q, kv, sink, idx = _inputs(seed + B, B, T, K, N, kv_scale=kv_scale)
         out = torch.empty(B, T, 64, 512, dtype=dtype, device="cuda")
         code, scratch = _noalloc(lib, q, kv, sink, idx, out)
         assert code == 0, sa.SAError(code, "sa_sparse_attn_noalloc")
@@ -63,7 +65,13 @@ def test_noalloc_matches_workspace_entry_two_calls(B, T, K, N, dtype):
         assert lib_code == 0
         ref = sa.sparse_attn(q, kv, sink, idx, 512 ** -0.5, out_dtype=dtype, check=True)
         torch.cuda.synchronize()
-        compare(out.double().cpu().numpy(), ref.double().cpu().numpy(), f"call {call}")
+        compare(out.double().cpu().numpy() / kv_scale, ref.double().cpu().numpy() / kv_scale,
+                f"call {call}")
+        if kv_scale != 1.0:
+            # and against the oracle itself
+            want, bad = oracle.sparse_attn(q.cpu(), kv.cpu(), sink.cpu(), idx.cpu(), 512 ** -0.5)
+            assert bad == 0
+            compare(out.double().cpu().numpy() / kv_scale, want / kv_scale, f"call {call} vs oracle")
 
 
 def test_noalloc_reports_errors_per_call():
