@@ -718,6 +718,27 @@ __device__ __forceinline__ int head_exponent(float max_abs)
     return min(15 - e, 127);
 }
 
+// Write NV heads' values of one feature (this lane's `f`, one value per head
+// in v) as bf16 into out[head][f] rows of D features, without staging: the two
+// lanes of an adjacent-feature pair swap half of their values, so that the
+// even lane writes features (f, f + 1) of the first NV/2 heads and the odd
+// lane those of the last NV/2, as 4-byte words (a warp's store covers two
+// contiguous 64-byte runs).
+template <int NV>
+__device__ __forceinline__ void store_bf16_pairs(uint16_t *out_h0, int f, const float (&v)[NV], int lane)
+{
+    const bool odd = lane & 1;
+    const int f0 = f & ~1;
+#pragma unroll
+    for (int i = 0; i < NV / 2; ++i) {
+        const float send = odd ? v[i] : v[NV / 2 + i];
+        const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+        const int h = odd ? NV / 2 + i : i;
+        const uint32_t w = odd ? pack_bf16x2(got, v[NV / 2 + i]) : pack_bf16x2(v[i], got);
+        *reinterpret_cast<uint32_t *>(out_h0 + (size_t)h * D + f0) = w;
+    }
+}
+
 template <int P>
 __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl, const Seg &s,
                               int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
@@ -750,14 +771,15 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     if (t < P && t != (int)me)
         mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
     // each head's largest |O| over this piece's 512 features: per warp over its
-    // 32 features of two tiles, then over the eight warps
+    // 32 features of two tiles (one redux per head on the bit patterns, which
+    // order as the values do for non-negative floats), then over the eight warps
     const int wi = t >> 5;
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
-        float mx[32];
+        uint32_t a[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            mx[i] = 0.f;
+            a[i] = 0u;
         if (nc > 0) {
 #pragma unroll 1
             for (int e = 0; e < 2; ++e) {
@@ -766,10 +788,17 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    mx[i] = fmaxf(mx[i], fabsf(__uint_as_float(v[i])));
+                    a[i] = max(a[i], v[i] & 0x7FFFFFFFu);
             }
         }
-        xmax[wi * 64 + 32 * hh + lane] = warp_reduce32<true>(mx, lane);
+        uint32_t mine = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t m = __reduce_max_sync(0xffffffffu, a[i]);
+            if (lane == i)
+                mine = m;
+        }
+        xmax[wi * 64 + 32 * hh + lane] = __uint_as_float(mine);
     }
     bar_sync(1, SMX_THREADS);
     if (t < H) {
@@ -864,8 +893,6 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     }
     bar_sync(1, SMX_THREADS);
 
-    // each half stages its tile as [HP heads][128 features] bf16 in its half of the P buffer
-    uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P) + hf * (HP * 128);
 #pragma unroll 1
     for (int e = 0; e < 2; ++e) {
         const int d = 2 * hf + e;
@@ -916,22 +943,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             for (int i = 0; i < HP; ++i)
                 po[i * D] = o[i];
         } else {
-#pragma unroll
-            for (int i = 0; i < HP; ++i)
-                stg[i * 128 + fl] = __bfloat16_as_ushort(__float2bfloat16_rn(o[i]));
-            bar_sync(2 + hf, 128);
-            // 256-byte head rows of this tile with 16-byte stores
-            const int tt = t & 127;
-            uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + (size_t)(me * HP) * D + 128 * d) * 2;
-            const uint8_t *sp = reinterpret_cast<const uint8_t *>(stg);
-#pragma unroll
-            for (int j = 0; j < HP / 8; ++j) {
-                const int c = tt + 128 * j;   // 16-byte piece c: head c / 16, part c % 16
-                const int h = c >> 4, part = c & 15;
-                const uint4 val = *reinterpret_cast<const uint4 *>(sp + h * 256 + part * 16);
-                *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = val;
-            }
-            bar_sync(2 + hf, 128);
+            store_bf16_pairs<HP>(reinterpret_cast<uint16_t *>(p.out) + (size_t)s.q * (H * D) + (size_t)(me * HP) * D, f,
+                                 o, lane);
         }
     }
     return true;
@@ -1116,7 +1129,6 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
 
         // epilogue: thread (qd, lane, hf) owns feature 128d + 32qd + lane of heads hb .. hb + 31
         const bool rope_here = p.rope_dim > 0;
-        uint16_t *stg = reinterpret_cast<uint16_t *>(smem + OFF_P);
 #pragma unroll 1
         for (int d = 0; d < 4; ++d) {
             const int dim = 128 * d + row;
@@ -1150,22 +1162,12 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 for (int i = 0; i < 32; ++i)
                     po[i * D] = __uint_as_float(u[i]);
             } else {
-                // stage the tile as [64 heads][128 features] bf16 in the P buffer
-                // (free once the last PV is done), then write whole 256-byte head
-                // rows with 16-byte stores
+                float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    stg[(hb + i) * 128 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(u[i])));
-                bar_sync(1, SMX_THREADS);
-                uint8_t *gout = reinterpret_cast<uint8_t *>(p.out) + ((size_t)s.q * (H * D) + 128 * d) * 2;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int c = t + SMX_THREADS * j;   // 16-byte piece c: head c / 16, part c % 16
-                    const int h = c >> 4, part = c & 15;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(smem + OFF_P + h * 256 + part * 16);
-                    *reinterpret_cast<uint4 *>(gout + (size_t)h * D * 2 + part * 16) = v;
-                }
-                bar_sync(1, SMX_THREADS);
+                    v[i] = __uint_as_float(u[i]);
+                store_bf16_pairs<32>(reinterpret_cast<uint16_t *>(p.out) + (size_t)s.q * (H * D) + (size_t)hb * D, dim,
+                                     v, lane);
             }
         }
         if (nc > 0) {
@@ -1209,6 +1211,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);
     }
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Programmatic dependent launch: everything above may overlap the previous
+    // kernel in the stream; every global memory access below waits for it to
+    // complete.  The next kernel may be scheduled as this grid's CTAs leave.
+    griddep_wait();
+    griddep_launch_dependents();
     // the control warp starts copying the sinks and the first index list now,
     // so that their latency overlaps the rest of the set-up; it waits for the
     // copies, scales the sinks and publishes both with the first list
@@ -1222,10 +1233,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
             stage_list(p, s, sbase + OFF_RAW, lane);
         else
             cp_async_commit();
-    }
-    if (warp == WARP_MMA) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
@@ -1329,19 +1336,28 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st)
     p.pieces = s.pieces;
     if (s.grid == 0)
         return cudaSuccess;
-    // the pieces of one query form a cluster (they merge through distributed shared memory)
+    // the pieces of one query form a cluster (they merge through distributed
+    // shared memory); programmatic dependent launch lets the set-up overlap
+    // the previous kernel in the stream
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)s.grid);
     cfg.blockDim = dim3(attn::THREADS);
     cfg.dynamicSmemBytes = attn::SMEM_BYTES;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)s.pieces;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (s.split) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)s.pieces;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = s.split ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
