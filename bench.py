@@ -3,12 +3,20 @@
 Default (our arm): the decode workload (B=64 queries, 640-entry index lists,
 8192-token context at ratio 2 -> 4224 latent rows per batch row), timed as one
 `sa_sparse_attn` call per step over rotating input sets whose total size
-exceeds L2, replayed from a CUDA graph.  Prints ONE JSON line.  The other
-lines are measured too and reported under "workloads": long-context decode,
-prefill, the fused tail (attention, inverse RoPE, grouped wo_a), the block
-tail (plus wo_b), decode with fp4 compressed rows, the fused tail with an
-fp8 wo_a, and the top-k selection (8192 rows x 4096 scores -> 512).
---extra NAME times one of them alone.
+exceeds L2, replayed from a CUDA graph.  Prints ONE compact JSON line (floats
+to four significant digits, the per-workload entries last).  Besides the
+contract's keys it carries, under "workloads", the other lines: long-context
+decode, prefill, the fused tail (attention, inverse RoPE, grouped wo_a), the
+block tail (plus wo_b), the top-k selection (8192 rows x 4096 scores -> 512),
+decode with fp4 compressed rows and the fused tail with an fp8 wo_a.  Each
+entry: "ms" per call, "qps" (queries/s; "rows_per_s" for top-k), the roofline
+("bound" hbm or tensor; "ach" achieved, GB/s or TFLOP/s; "peak"; "frac";
+"traffic", measured DRAM bytes per launch of the dominant kernel, or null;
+"peak_kind" burst or sustained for tensor-bound lines) and "cpu", the fp64
+oracle's queries/s (rows/s) on the host cores on the same inputs (whole calls
+for decode, else a block of queries scaled by flops).  A tensor-bound line is
+divided by the burst bf16 peak when its timed region is under a second, by
+the sustained one otherwise.  --extra NAME times one additional line alone.
 
 --impl reference: the fp64 CPU oracle, timed as it stands on the host cores
 on a bounded sample of the same workload (the only reference this path has).
@@ -165,6 +173,26 @@ def peaks() -> dict:
             "source": "fallback"}
 
 
+def tensor_peak(pk: dict, timed_s: float):
+    """The bf16 peak a tensor-bound line is divided by: the burst figure for a
+    timed region under a second (a kernel timed alone), the sustained one for a
+    longer region (a kernel running under the power cap)."""
+    if timed_s < 1.0:
+        return pk["bf16_tflops"], f"{pk['source']} burst bf16"
+    return pk["bf16_tflops_sustained"], f"{pk['source']} sustained bf16"
+
+
+def sig(x, digits=4):
+    """Round every float in a JSON-able structure to `digits` significant digits."""
+    if isinstance(x, float):
+        return float(f"{x:.{digits}g}")
+    if isinstance(x, dict):
+        return {k: sig(v, digits) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [sig(v, digits) for v in x]
+    return x
+
+
 def l2_bytes() -> int:
     try:
         return int(torch.cuda.get_device_properties(0).L2_cache_size)
@@ -260,7 +288,7 @@ def launches_per_call(wl: I.Workload, num_sms: int) -> int:
     return 1 + (1 if wl.tail else 0) + (1 if wl.wo_b else 0)
 
 
-def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_sets=None):
+def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_sets=None, cpu_s: float = 0.0):
     import sparse_latent_attention_02_gb300 as sa
     wl = I.WORKLOADS[name]
     sets = sets_for(wl, dev, n_sets=n_sets)
@@ -314,6 +342,8 @@ def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_se
     }
     if with_e2e:
         res["e2e"] = bench_e2e(wl, sets[0], steps, warmup, dev)
+    if cpu_s > 0:
+        res["cpu"] = cpu_rate(name, sets[0], cpu_s)
     del sets, outs, fns
     torch.cuda.empty_cache()
     return res
@@ -389,7 +419,7 @@ def bench_e2e(wl: I.Workload, x: dict, steps: int, warmup: int, dev) -> dict:
                     f"output copied back; copies, calls and read-backs pipelined on three streams"}
 
 
-def bench_topk(steps: int, warmup: int, dev, pk: dict) -> dict:
+def bench_topk(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 0.0) -> dict:
     """Top-k selection of 512 of 4096 compressed positions for the 8192 queries
     of the prefill workload (scores N(0,1), each query's visible prefix
     causal): one call per step, inputs rotating over sets larger than L2."""
@@ -409,13 +439,22 @@ def bench_topk(steps: int, warmup: int, dev, pk: dict) -> dict:
     step_s = secs / steps
     nbytes = rows * L * 4 + rows * k * 4
     gbs = nbytes / step_s / 1e9
-    return {"workload": f"topk: {rows} rows x {L} positions -> {k}", "ms_per_step": step_s * 1e3,
-            "rows_per_s": rows / step_s, "gbs": gbs, "bytes_per_step": nbytes,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "peak_note": f"{pk['source']} HBM copy"}}
+    res = {"ms_per_step": step_s * 1e3, "rows_per_s": rows / step_s, "bytes_per_step": nbytes,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "traffic": None}}
+    if cpu_s > 0:
+        import oracle
+        n = 256
+        sc = sets[0][0][:n].cpu().numpy()
+        t0 = time.time()
+        oracle.topk_indices(sc, k, offset=128)
+        dt = time.time() - t0
+        res["cpu"] = {"value": n / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                      "sample": f"{n} rows, {dt:.1f} s"}
+    return res
 
 
-def bench_decode_fp4(steps: int, warmup: int, dev, pk: dict) -> dict:
+def bench_decode_fp4(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 0.0) -> dict:
     """The decode workload with its compressed cache stored as fp4 (e2m1 codes
     and an E4M3 scale per 16 features, 288 bytes per row) next to the bf16
     window: the same lists, the two-source fp4 call, rotating input sets larger
@@ -450,15 +489,28 @@ def bench_decode_fp4(steps: int, warmup: int, dev, pk: dict) -> dict:
     nbytes = (win_rows * D * 2 + fp4_rows * (D // 2 + D // 16) + wl.n_queries * wl.H * D * 4
               + idx.numel() * 4 + wl.H * 4)
     gbs = nbytes / step_s / 1e9
-    return {"workload": f"decode with fp4 compressed rows: B={wl.B} K={wl.K} ({wl.W} bf16 window + "
-                        f"{wl.C} fp4 compressed rows per batch row)",
-            "ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "gbs": gbs,
-            "bytes_per_step": nbytes,
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "peak_note": f"{pk['source']} HBM copy"}}
+    res = {"ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "bytes_per_step": nbytes,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "traffic": None}}
+    if cpu_s > 0:
+        import oracle
+        x, win, c, sc = sets[0][:4]
+        args = (x["q"].cpu(), win.cpu(), wl.W, c.cpu().numpy(), sc.cpu().numpy(), wl.C, x["sink"].cpu(),
+                x["idx"].cpu(), wl.scale)
+        oracle.sparse_attn_two_source_fp4(*args)
+        done, t0 = 0, time.time()
+        while True:
+            oracle.sparse_attn_two_source_fp4(*args)
+            done += 1
+            if time.time() - t0 >= cpu_s or done >= 1000:
+                break
+        dt = time.time() - t0
+        res["cpu"] = {"value": wl.n_queries * done / dt, "unit": "queries/s", "cores": oracle.threads(0),
+                      "kind": "oracle", "sample": f"{done} whole calls"}
+    return res
 
 
-def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict) -> dict:
+def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 0.0) -> dict:
     """The fused-tail workload (attention, inverse RoPE, grouped wo_a) with wo_a
     kept as an fp8 checkpoint (E4M3 + an fp32 scale per 128 x 128 block,
     decoded by the call into a bf16 workspace copy): same inputs and flops as
@@ -482,45 +534,113 @@ def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict) -> dict:
     step_s = secs / steps
     flops = float(np.mean([algorithmic(wl, x["idx"])["flops"] for x in sets]))
     tflops = flops / step_s / 1e12
-    w_bytes = sets[0]["w8"].numel() + sets[0]["w8_scales"].numel() * 4
+    peak, note = tensor_peak(pk, secs)
+    res = {"ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "flops_per_step": int(flops),
+           "gpu_launches": 3 * steps,
+           "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                        "frac": tflops / peak, "traffic": None, "peak_note": note}}
+    if cpu_s > 0:
+        import oracle
+        x = dict(sets[0])
+        t0 = time.time()
+        w8 = x["w8"].cpu().numpy()
+        x["wo_a"] = torch.from_numpy(oracle.dequant_fp8_weight(w8.reshape(-1, w8.shape[-1]),
+                                                                x["w8_scales"].cpu().numpy()).view(np.int16)
+                                     ).view(torch.bfloat16).reshape(w8.shape)
+        deq = time.time() - t0
+        r = cpu_rate("fused_tail", x, cpu_s)
+        call_s = wl.n_queries / r["value"] + deq
+        res["cpu"] = {"value": wl.n_queries / call_s, "unit": "queries/s", "cores": r["cores"], "kind": "oracle",
+                      "sample": r["sample"] + f", + weight decoding {deq:.1f} s"}
     del sets, fns
     torch.cuda.empty_cache()
-    return {"workload": f"fused tail with an fp8 wo_a: B={wl.B} T={wl.T} K={wl.K}, wo_a E4M3 "
-                        f"[{wl.G}, {wl.R}, {wl.H * wl.D // wl.G}] + 128x128 block scales ({w_bytes} bytes)",
-            "ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "tflops": tflops,
-            "flops_per_step": int(flops), "gpu_launches": 3 * steps,
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops_sustained"],
-                         "unit": "TFLOP/s", "frac": tflops / pk["bf16_tflops_sustained"],
-                         "peak_note": f"{pk['source']} sustained bf16 (the products are bf16)"}}
+    return res
 
 
 # the additional lines that are not attention workloads, by name
 EXTRA_LINES = {
-    "topk": lambda steps, warmup, dev, pk: bench_topk(steps, warmup, dev, pk),
-    "decode_fp4": lambda steps, warmup, dev, pk: bench_decode_fp4(steps, warmup, dev, pk),
-    "fused_tail_fp8": lambda steps, warmup, dev, pk: bench_fused_tail_fp8(steps, warmup, dev, pk),
+    "topk": bench_topk,
+    "decode_fp4": bench_decode_fp4,
+    "fused_tail_fp8": bench_fused_tail_fp8,
 }
 
 
-def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
-    """The fp64 oracle, as it stands, on the host cores: whole decode steps
-    (all queries of one input set) repeated until about `budget_s` seconds."""
+def _oracle_chain(wl: I.Workload, q, kv, sink, idx, wo_a=None, wo_b=None):
+    """The oracle's steps for a block of queries (q [1, n, H, D] etc. on the
+    host): attention, and for the tails inverse RoPE, wo_a and wo_b."""
+    import oracle
+    o, _ = oracle.sparse_attn(q, kv, sink, idx, wl.scale)
+    if wl.tail:
+        n = q.shape[1]
+        pos = np.arange(n)   # positions only shift the angles; the work is the same
+        o = oracle.inverse_rope(o.reshape(n, wl.H, wl.D), pos, wl.rope_dim, wl.theta)
+        y = oracle.wo_a(o.reshape(n, wl.G, -1), wo_a)
+        if wl.wo_b:
+            oracle.wo_b(y.reshape(n, -1), wo_b)
+
+
+def cpu_rate(name: str, x: dict, budget_s: float) -> dict:
+    """The fp64 oracle, as it stands, on the host cores on one input set of a
+    workload (x: its tensors, on any device): whole calls repeated for about
+    `budget_s` when a call is short (the decode workloads), else one contiguous
+    block of queries of the first batch element (attention and, for the tails,
+    the projections), scaled to the whole call by algorithmic flops.  Returns
+    queries/s, the threads used and what was timed."""
     import oracle
     wl = I.WORKLOADS[name]
-    x = I.make_inputs(wl, seed=0)
     cores = oracle.threads(0)
-    oracle.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)   # warm
-    done, t0 = 0, time.time()
-    while True:
-        oracle.sparse_attn(x["q"], x["kv"], x["sink"], x["idx"], wl.scale)
-        done += 1
-        if time.time() - t0 >= budget_s or done >= 1000:
-            break
+    cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in x.items()
+           if k in ("q", "kv", "sink", "idx", "wo_a", "wo_b")}
+    if wl.T == 1:   # decode: whole calls
+        oracle.sparse_attn(cpu["q"], cpu["kv"], cpu["sink"], cpu["idx"], wl.scale)
+        done, t0 = 0, time.time()
+        while True:
+            oracle.sparse_attn(cpu["q"], cpu["kv"], cpu["sink"], cpu["idx"], wl.scale)
+            done += 1
+            if time.time() - t0 >= budget_s or done >= 1000:
+                break
+        secs = time.time() - t0
+        return {"value": wl.n_queries * done / secs, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                "sample": f"{done} whole calls"}
+    n = 512 if not wl.tail else (256 if not wl.wo_b else 128)
+    t_a = wl.T // 2
+    blk = dict(q=cpu["q"][:1, t_a:t_a + n], kv=cpu["kv"][:1], sink=cpu["sink"], idx=cpu["idx"][:1, t_a:t_a + n])
+    t0 = time.time()
+    _oracle_chain(wl, blk["q"], blk["kv"], blk["sink"], blk["idx"], cpu.get("wo_a"), cpu.get("wo_b"))
     secs = time.time() - t0
-    return {"value": wl.n_queries * done / secs, "unit": "queries/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"{done} full {name} steps ({wl.n_queries} queries each), fp64, "
-                      f"{secs:.1f} s on {cores} host threads"}
+    full = algorithmic(wl, cpu["idx"])["flops"]
+    part = algorithmic(I.scaled(wl, B=1, T=n), blk["idx"])["flops"]
+    call_s = secs * full / part
+    return {"value": wl.n_queries / call_s, "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} queries (t {t_a}..{t_a + n - 1}), {secs:.1f} s, scaled by flops"}
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
+    """The headline's oracle baseline on a fresh host input set."""
+    x = I.make_inputs(I.WORKLOADS[name], seed=0)
+    return cpu_rate(name, x, budget_s)
+
+
+def _entry(r: dict) -> dict:
+    """A workload's compact entry in the printed line: milliseconds per call,
+    throughput, the roofline (achieved in GB/s for "hbm", TFLOP/s for
+    "tensor"; peak; fraction; measured DRAM bytes per launch of the dominant
+    kernel or null) and the oracle's rate on the host cores."""
+    rf = r["roofline"]
+    e = {"ms": r["ms_per_step"]}
+    if "queries_per_s" in r:
+        e["qps"] = r["queries_per_s"]
+    if "rows_per_s" in r:
+        e["rows_per_s"] = r["rows_per_s"]
+    e.update({"bound": rf["bound"], "ach": rf["achieved"], "peak": rf["peak"], "frac": rf["frac"],
+              "traffic": rf.get("traffic")})
+    if rf.get("peak_note", "").find("burst") >= 0:
+        e["peak_kind"] = "burst"
+    elif rf["bound"] == "tensor":
+        e["peak_kind"] = "sustained"
+    if r.get("cpu"):
+        e["cpu"] = r["cpu"]["value"]
+    return e
 
 
 def run_ours(args):
@@ -532,11 +652,12 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
+    cpu_s = args.cpu_seconds if world == 1 else 0.0
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     head = bench_workload(args.workload, args.steps, args.warmup, dev,
-                          with_e2e=not args.no_e2e and world == 1, n_sets=args.sets)
+                          with_e2e=not args.no_e2e and world == 1, n_sets=args.sets, cpu_s=cpu_s)
     secs, units = aggregate_over_ranks(head["ms_per_step"] * 1e-3 * args.steps,
                                        head["queries_per_s"] * head["ms_per_step"] * 1e-3 * args.steps)
     head["job_queries_per_s"] = units / secs
@@ -548,29 +669,29 @@ def run_ours(args):
         return
     extra = {}
     if not args.headline_only and world == 1:
+        per_line_cpu = min(cpu_s, 3.0)
         for name in ("long_decode", "prefill", "fused_tail", "block_tail"):
             steps = max(3, min(args.steps, 20))
-            r = bench_workload(name, steps, max(args.warmup, 3), dev, with_e2e=False)
-            r["clocks"] = sampler.summary(*r.pop("window"))
+            r = bench_workload(name, steps, max(args.warmup, 3), dev, with_e2e=False, cpu_s=per_line_cpu)
+            sampler.summary(*r.pop("window"))
             if name in ("prefill", "fused_tail", "block_tail"):
-                r["roofline"] = {"bound": "tensor", "achieved": r["tflops"],
-                                 "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                                 "frac": r["tflops"] / pk["bf16_tflops_sustained"],
-                                 "traffic": measured_traffic(name),
-                                 "peak_note": f"{pk['source']} sustained bf16"}
+                peak, note = tensor_peak(pk, r["ms_per_step"] * 1e-3 * steps)
+                r["roofline"] = {"bound": "tensor", "achieved": r["tflops"], "peak": peak, "unit": "TFLOP/s",
+                                 "frac": r["tflops"] / peak, "traffic": measured_traffic(name), "peak_note": note}
             else:
-                r["roofline"] = {"bound": "hbm", "achieved": r["gbs"], "peak": pk["hbm_gbs"],
-                                 "unit": "GB/s", "frac": r["gbs"] / pk["hbm_gbs"],
-                                 "traffic": measured_traffic(name),
-                                 "peak_note": f"{pk['source']} HBM copy"}
-            extra[name] = r
-        extra["topk"] = bench_topk(max(3, min(args.steps, 50)), max(args.warmup, 3), dev, pk)
-        extra["decode_fp4"] = bench_decode_fp4(max(3, min(args.steps, 200)), max(args.warmup, 3), dev, pk)
-        extra["fused_tail_fp8"] = bench_fused_tail_fp8(max(3, min(args.steps, 20)), max(args.warmup, 3), dev, pk)
+                r["roofline"] = {"bound": "hbm", "achieved": r["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                 "frac": r["gbs"] / pk["hbm_gbs"], "traffic": measured_traffic(name)}
+            extra[name] = _entry(r)
+        extra["topk"] = _entry(bench_topk(max(3, min(args.steps, 50)), max(args.warmup, 3), dev, pk, per_line_cpu))
+        extra["decode_fp4"] = _entry(bench_decode_fp4(max(3, min(args.steps, 200)), max(args.warmup, 3), dev, pk,
+                                                      per_line_cpu))
+        extra["fused_tail_fp8"] = _entry(bench_fused_tail_fp8(max(3, min(args.steps, 20)), max(args.warmup, 3), dev,
+                                                              pk, per_line_cpu))
     sampler.stop()
     e2e = head.pop("e2e", None)
-    cpu = (cpu_baseline(args.workload, budget_s=args.cpu_seconds)
-           if args.cpu_seconds > 0 and world == 1 else None)
+    if e2e:
+        e2e.pop("note", None)
+    cpu = head.pop("cpu", None)
     line = {
         "metric": METRIC, "value": head["job_queries_per_s"], "unit": "queries/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -578,24 +699,20 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: B={head['B']} T={head['T']} H=64 D=512 "
                                f"N={head['N']} K={head['K']}",
-                   "parallelism": f"replicas only ({world} independent GPU replica"
-                                  f"{'s' if world > 1 else ''}, no collective on the data path)",
-                   "l2": f"inputs rotate over {head['input_sets']} independent sets "
-                         f"(> 2x L2 per rotation)",
-                   "timing": "CUDA graph of `steps` calls, CUDA events on its stream"},
+                   "parallelism": f"replicas only ({world} GPU{'s' if world > 1 else ''}, no collective)",
+                   "l2": f"{head['input_sets']} rotating input sets, > 2x L2"},
         "gbs": head["gbs"], "tflops": head["tflops"],
         "roofline": {"bound": "hbm", "achieved": head["gbs"], "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": head["gbs"] / pk["hbm_gbs"],
                      "traffic": measured_traffic(args.workload),
-                     "note": f"peak = {pk['source']} HBM copy; achieved = algorithmic bytes "
-                             f"({head['bytes_per_step']} per call) / call duration"},
+                     "bytes_per_call": head["bytes_per_step"]},
         "e2e": e2e,
         "gpu_launches": head["gpu_launches"] * world,
-        "clocks": clocks,
+        "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons") if k in clocks},
         "cpu_baseline": cpu,
         "workloads": extra,
     }
-    print(json.dumps(line))
+    print(json.dumps(sig(line), separators=(",", ":")))
     barrier()
 
 
@@ -632,7 +749,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--headline-only", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+    ap.add_argument("--cpu-seconds", type=float, default=6.0,
                     help="CPU-baseline budget; 0 skips it (profiling runs)")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(I.WORKLOADS),
                     help="workload of the headline line (default: decode)")
@@ -649,8 +766,9 @@ def main():
         sa.build()
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        print(json.dumps({"extra": args.extra,
-                          **EXTRA_LINES[args.extra](args.steps, args.warmup, dev, peaks())}))
+        print(json.dumps(sig({"extra": args.extra,
+                              **EXTRA_LINES[args.extra](args.steps, args.warmup, dev, peaks(),
+                                                        min(args.cpu_seconds, 3.0))})))
         return
     rank, world, local = dist_env()
     if args.impl == "reference":

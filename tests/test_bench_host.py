@@ -98,3 +98,34 @@ def test_reference_arm_prints_one_line_on_rank_zero_only():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["config"]["workload"].startswith("decode: B=64 T=1")
+
+
+def test_tensor_peak_is_burst_for_short_regions():
+    pk = {"hbm_gbs": 6784.8, "bf16_tflops": 1890.6, "bf16_tflops_sustained": 1687.3, "source": "measured"}
+    assert bench.tensor_peak(pk, 0.03)[0] == 1890.6 and "burst" in bench.tensor_peak(pk, 0.03)[1]
+    assert bench.tensor_peak(pk, 4.0)[0] == 1687.3 and "sustained" in bench.tensor_peak(pk, 4.0)[1]
+
+
+def test_printed_line_rounding_and_entries():
+    assert bench.sig({"a": 1234.5678, "b": [0.000123456, 7], "c": "x"}) == {"a": 1235.0, "b": [0.0001235, 7], "c": "x"}
+    r = {"ms_per_step": 1.2345678, "queries_per_s": 6.5e6, "cpu": {"value": 530.0},
+         "roofline": {"bound": "tensor", "achieved": 500.0, "peak": 1890.6, "frac": 0.2645, "traffic": None,
+                      "peak_note": "measured burst bf16"}}
+    e = bench._entry(r)
+    assert e == {"ms": 1.2345678, "qps": 6.5e6, "bound": "tensor", "ach": 500.0, "peak": 1890.6, "frac": 0.2645,
+                 "traffic": None, "peak_kind": "burst", "cpu": 530.0}
+
+
+def test_oracle_rate_scales_a_block_by_flops():
+    """The per-workload oracle baseline: whole calls for decode, a block of
+    queries scaled by algorithmic flops otherwise (a positive rate, its sample
+    stated)."""
+    wl = I.scaled(I.WORKLOADS["prefill"], T=1100)
+    I.WORKLOADS["_tiny_prefill"] = wl
+    try:
+        x = I.make_inputs(wl, seed=0)
+        r = bench.cpu_rate("_tiny_prefill", x, 1.0)
+        assert r["value"] > 0 and r["kind"] == "oracle" and "scaled by flops" in r["sample"]
+        assert r["sample"].startswith("512 queries (t 550..1061)")
+    finally:
+        del I.WORKLOADS["_tiny_prefill"]
