@@ -90,9 +90,8 @@ constexpr uint32_t OFF_SEGN = OFF_AUX + 64 * 4;        // int [2] list lengths
 constexpr uint32_t OFF_BAR = OFF_SEGN + 16;            // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;        // [0] TMEM base, [1] abort flag
 constexpr uint32_t OFF_RAW = OFF_MISC + 64;           // int32 [SA_MAX_K] list as read from idx
-constexpr uint32_t OFF_XSTAT = OFF_RAW + 4 * SA_MAX_K;   // float [pieces][3][64 / pieces] peers' (m, l, k)
-constexpr uint32_t OFF_XSEND = OFF_XSTAT + 3 * 64 * 4;   // float [3][64 / pieces] (m, l, k) being sent
-constexpr uint32_t OFF_SINK = OFF_XSEND + 3 * 64 * 4;    // float [64] sink * log2(e)
+constexpr uint32_t OFF_XSTAT = OFF_RAW + 4 * SA_MAX_K;   // float [pieces][2][64 / pieces] peers' (m, l)
+constexpr uint32_t OFF_SINK = OFF_XSTAT + 2 * 64 * 4;    // float [64] sink * log2(e)
 constexpr uint32_t SMEM_USED = OFF_SINK + 64 * 4;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -110,7 +109,7 @@ enum : uint32_t {
     B_LEMPTY0 = B_LFULL0 + 2,
     B_DONE = B_LEMPTY0 + 2,
     B_XRDY,      // split schedule: every peer's chunk buffer is free to receive
-    B_XFULL,     // split schedule: every peer's partial for this CTA's heads has arrived (bytes)
+    B_XFULL,     // split schedule: every peer's partial for this CTA's heads has arrived
     NUM_BARS
 };
 constexpr uint32_t LEMPTY_ARRIVALS = NUM_GATHER_WARPS + 1 + NUM_SOFTMAX_WARPS;   // gather warps, MMA, softmax warps
@@ -687,36 +686,19 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 
 // Split schedule: the P pieces of one query's list run as one cluster, and
 // CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  Every
-// CTA sends each peer its unnormalised O^T columns for that peer's heads, as
-// fp16 pairs of adjacent heads after an exact per-head power-of-two scaling
-// 2^k (k = head_exponent of the head's largest |O| in this piece), together
-// with its (m, l, k) for those heads, into the peer's chunk buffer: it stages
-// them in its own slot of its own chunk buffer (the slot no peer writes) and
-// moves them with one bulk shared-to-shared copy per peer, which completes on
-// the peer's XFULL barrier.  A CTA offers its buffer (arrives on each peer's
-// XRDY barrier) once its own last PV product is done.  The receiver merges
-// the pieces:
+// CTA writes each peer its unnormalised O^T columns for that peer's heads, in
+// fp32 straight from TMEM into the peer's chunk buffer (st.shared::cluster;
+// slot `me` of P slots, pairs of adjacent heads per feature), together with
+// its (m, l) for those heads, then arrives on the peer's XFULL barrier with
+// release semantics.  A CTA offers its buffer (arrives on each peer's XRDY
+// barrier) once its own last PV product is done.  The receiver merges the
+// pieces:
 //   M = max_r m_r (each m_r starts at the sink),  w_r = 2^(m_r - M),
-//   o = sum_r w_r 2^-k_r (2^k_r O_r) / (sum_r w_r l_r + 2^(sink*log2e - M))
-// then applies the inverse RoPE when asked and writes its heads.  Softmax
-// warps only: warp (quarter qd, half hf) handles features 128d + 32qd + lane
-// of tiles d = 2hf, 2hf + 1.  False when a wait ran out.
-//
-// Exponent of the scaling that brings a head's largest |O| = f * 2^e, f in
-// [0.5, 1), to f * 2^15, inside fp16's range (65504) with its full 11-bit
-// precision, whatever the magnitude of kv or of the row sum: k = 15 - e,
-// capped at 127 so that 2^k stays a finite float (a head whose largest
-// entry is below 2^-112 keeps less precision, at a magnitude that cannot
-// matter).  0 for an all-zero head (or a non-finite one).  The scaling is
-// exact, so integer-valued partials (the index-probe case) stay exact.
-__device__ __forceinline__ int head_exponent(float max_abs)
-{
-    if (!(max_abs > 0.f) || !(max_abs <= 3.402823466e38f))
-        return 0;
-    int e;
-    (void)frexpf(max_abs, &e);
-    return min(15 - e, 127);
-}
+//   o = sum_r w_r O_r / (sum_r w_r l_r + 2^(sink*log2e - M))
+// then applies the inverse RoPE when asked and writes its heads.  fp32 keeps
+// the partials' full range and precision whatever the magnitude of kv.
+// Softmax warps only: warp (quarter qd, half hf) handles features
+// 128d + 32qd + lane of tiles d = 2hf, 2hf + 1.  False when a wait ran out.
 
 // Write NV heads' values of one feature (this lane's `f`, one value per head
 // in v) as bf16 into out[head][f] rows of D features, without staging: the two
@@ -744,92 +726,33 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                               int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
 {
     constexpr int HP = H / P;
-    // one piece's O for HP heads, [HP][512], sent as fp16 after an exact
-    // per-head power-of-two scaling (largest |entry| in [2^14, 2^15))
-    constexpr uint32_t SLOT_BYTES = HP * D * 2;
-    constexpr uint32_t STAT_BYTES = 3 * HP * 4;      // its (m, l, k) for HP heads
-    static_assert(STAT_BYTES % 16 == 0, "bulk copy size");
-    constexpr int COPY_PARTS = 8;                    // a slot goes as 8 copies issued by 8 threads
+    // one piece's O for HP heads: fp32 [HP / 2][512] pairs of heads (2j, 2j + 1) per feature
+    constexpr uint32_t SLOT_BYTES = HP * D * 4;
+    static_assert(P * SLOT_BYTES <= KV_BYTES, "receive slots fit the chunk buffer");
     const uint32_t me = cluster_ctarank();
     const uint32_t bar0 = sbase + OFF_BAR;
     const float *m_s = reinterpret_cast<const float *>(smem + OFF_M);
     const float *lt = reinterpret_cast<const float *>(smem + OFF_AUX);   // this piece's row sums
-    const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);
+    const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);   // [P][2][HP] peers' (m, l)
     float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights, then [HP] 1/den
-    // in the P buffer (free once the last PV is done) while sending:
-    float *xmax = reinterpret_cast<float *>(smem + OFF_P);    // [8 warps][64] largest |O| per head
-    float *hscale = xmax + NUM_SOFTMAX_WARPS * 64;            // [64] 2^k
-    float *hexp = hscale + 64;                                // [64] k
-    // [P][HP / 2][512] pairs of heads (2j, 2j + 1) per feature
-    const __half2 *recv = reinterpret_cast<const __half2 *>(smem + OFF_KV);
-    __half2 *stage = reinterpret_cast<__half2 *>(smem + OFF_KV + me * SLOT_BYTES);
-    float *xsend = reinterpret_cast<float *>(smem + OFF_XSEND);
+    const float2 *recv = reinterpret_cast<const float2 *>(smem + OFF_KV);   // [P][HP / 2][512]
     const int fl = 32 * qd + lane;   // feature within a 128-feature tile
 
-    if (t == 0)
-        mbar_arrive_expect_tx(bar0 + 8 * B_XFULL, (P - 1) * (SLOT_BYTES + STAT_BYTES));
     if (t < P && t != (int)me)
         mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
-    // each head's largest |O| over this piece's 512 features: per warp over its
-    // 32 features of two tiles (one redux per head on the bit patterns, which
-    // order as the values do for non-negative floats), then over the eight warps
-    const int wi = t >> 5;
-#pragma unroll 1
-    for (int hh = 0; hh < 2; ++hh) {
-        uint32_t a[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            a[i] = 0u;
-        if (nc > 0) {
-#pragma unroll 1
-            for (int e = 0; e < 2; ++e) {
-                uint32_t v[32];
-                tmem_ld32(tl + TM_O + 64 * (2 * hf + e) + 32 * hh, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    a[i] = max(a[i], v[i] & 0x7FFFFFFFu);
-            }
-        }
-        uint32_t mine = 0u;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t m = __reduce_max_sync(0xffffffffu, a[i]);
-            if (lane == i)
-                mine = m;
-        }
-        xmax[wi * 64 + 32 * hh + lane] = __uint_as_float(mine);
-    }
-    bar_sync(1, SMX_THREADS);
-    if (t < H) {
-        float mx = 0.f;
-#pragma unroll
-        for (int w = 0; w < NUM_SOFTMAX_WARPS; ++w)
-            mx = fmaxf(mx, xmax[w * 64 + t]);
-        const int k = head_exponent(mx);
-        hscale[t] = ldexpf(1.f, k);
-        hexp[t] = (float)k;
-    }
     bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
     if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
         return false;
 
     // send: peer g gets columns g*HP .. g*HP + HP-1 of every 128-feature tile
-    bool first = true;
-    for (int g = 0; g < P; ++g) {
-        if (g == (int)me)
-            continue;
-        if (!first) {
-            // the previous copy has finished reading the staging slot
-            if (t < COPY_PARTS)
-                bulk_wait_read_all();
-            bar_sync(1, SMX_THREADS);
-        }
-        first = false;
+#pragma unroll 1
+    for (int gi = 1; gi < P; ++gi) {
+        const uint32_t g = (me + (uint32_t)gi) % (uint32_t)P;   // peers in a rotated order
+        const uint32_t dst = mapa_shared(sbase + OFF_KV + me * SLOT_BYTES, g);
         if (t < HP) {
-            xsend[t] = m_s[g * HP + t];
-            xsend[HP + t] = lt[g * HP + t];
-            xsend[2 * HP + t] = hexp[g * HP + t];
+            const uint32_t xs = mapa_shared(sbase + OFF_XSTAT + (me * 2 * HP + t) * 4, g);
+            st_cluster_f32(xs, m_s[g * HP + t]);
+            st_cluster_f32(xs + 4 * HP, lt[g * HP + t]);
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -847,24 +770,14 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             }
 #pragma unroll
             for (int i = 0; i < HP; i += 2)
-                stage[(i / 2) * D + 128 * d + fl] =
-                    __floats2half2_rn(__uint_as_float(v[i]) * hscale[g * HP + i],
-                                      __uint_as_float(v[i + 1]) * hscale[g * HP + i + 1]);
-        }
-        fence_proxy_async_smem();
-        bar_sync(1, SMX_THREADS);
-        if (t < COPY_PARTS) {
-            const uint32_t rbar = mapa_shared(bar0 + 8 * B_XFULL, (uint32_t)g);
-            const uint32_t off = OFF_KV + me * SLOT_BYTES + t * (SLOT_BYTES / COPY_PARTS);
-            bulk_copy_to_peer(mapa_shared(sbase + off, (uint32_t)g), sbase + off, SLOT_BYTES / COPY_PARTS, rbar);
-            if (t == 0)
-                bulk_copy_to_peer(mapa_shared(sbase + OFF_XSTAT + me * STAT_BYTES, (uint32_t)g),
-                                  sbase + OFF_XSEND, STAT_BYTES, rbar);
-            bulk_commit();
+                st_cluster_v2_b32(dst + (uint32_t)(((i / 2) * D + 128 * d + fl) * 8), v[i], v[i + 1]);
         }
     }
-    if (t < COPY_PARTS)
-        bulk_wait_read_all();
+    // every thread's stores are ordered before the arrivals below
+    fence_acq_rel_cluster();
+    bar_sync(1, SMX_THREADS);
+    if (t < P && t != (int)me)
+        mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XFULL, (uint32_t)t));
 
     ok = warp_wait_cluster(bar0 + 8 * B_XFULL, 0, abort_flag, p.timeout_ns, lane);
     if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
@@ -877,15 +790,14 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
 #pragma unroll
         for (int r = 0; r < P; ++r)
             if (r != (int)me)
-                M = fmaxf(M, xst[r * 3 * HP + t]);
+                M = fmaxf(M, xst[r * 2 * HP + t]);
         float den = 0.f;
 #pragma unroll
         for (int r = 0; r < P; ++r) {
-            const float mr = r == (int)me ? m_s[h] : xst[r * 3 * HP + t];
-            const float lr = r == (int)me ? lt[h] : xst[r * 3 * HP + HP + t];
+            const float mr = r == (int)me ? m_s[h] : xst[r * 2 * HP + t];
+            const float lr = r == (int)me ? lt[h] : xst[r * 2 * HP + HP + t];
             const float w = M == -INFINITY ? 0.f : ex2(mr - M);
-            // peers' O arrive multiplied by 2^k: undo it exactly
-            wts[r * HP + t] = r == (int)me ? w : ldexpf(w, -(int)xst[r * 3 * HP + 2 * HP + t]);
+            wts[r * HP + t] = w;
             den += w * lr;
         }
         den += M == -INFINITY ? 0.f : ex2(sl - M);
@@ -918,12 +830,12 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                 continue;
 #pragma unroll
             for (int i = 0; i < HP; i += 2) {
-                const float2 x = __half22float2(recv[(r * HP + i) / 2 * 512 + f]);
+                const float2 x = recv[(r * HP + i) / 2 * D + f];
                 o[i] += wts[r * HP + i] * x.x;
                 o[i + 1] += wts[r * HP + i + 1] * x.y;
             }
         }
-#pragma unroll
+        #pragma unroll
         for (int i = 0; i < HP; ++i)
             o[i] *= wts[P * HP + i];
         if (p.rope_dim > 0 && f >= D - p.rope_dim) {   // warp-uniform
@@ -1206,7 +1118,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         }
         mbar_init(bar0 + 8 * B_DONE, 1);
         mbar_init(bar0 + 8 * B_XRDY, p.split ? (uint32_t)(p.pieces - 1) : 1u);
-        mbar_init(bar0 + 8 * B_XFULL, 1);
+        mbar_init(bar0 + 8 * B_XFULL, p.split ? (uint32_t)(p.pieces - 1) : 1u);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);

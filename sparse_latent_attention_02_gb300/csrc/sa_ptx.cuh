@@ -133,6 +133,18 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_v2_b32(uint32_t addr, uint32_t a, uint32_t b)
+{
+    asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+// Orders this thread's earlier memory accesses (including stores into other
+// CTAs' shared memory) before its later ones, at cluster scope.
+__device__ __forceinline__ void fence_acq_rel_cluster()
+{
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 // Arrive on an mbarrier of another CTA of the cluster; releases this thread's
 // earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
@@ -171,31 +183,6 @@ __device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t pari
         }
     }
 }
-
-// Bulk copy from this CTA's shared memory to another CTA's shared memory in
-// the cluster; the bytes complete a transaction on that CTA's mbarrier.
-// Addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                  uint32_t mbar_cluster)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst_cluster),
-        "r"(src), "r"(bytes), "r"(mbar_cluster)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit()
-{
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Wait until the committed bulk copies have finished reading their sources.
-__device__ __forceinline__ void bulk_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
 
 // Every thread of every CTA of the cluster (warp-converged).
 __device__ __forceinline__ void cluster_sync()
