@@ -686,17 +686,19 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 
 // Split schedule: the P pieces of one query's list run as one cluster, and
 // CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  Every
-// CTA writes each peer its unnormalised O^T columns for that peer's heads, in
-// fp32 straight from TMEM into the peer's chunk buffer (st.shared::cluster;
-// slot `me` of P slots, pairs of adjacent heads per feature), together with
-// its (m, l) for those heads, then arrives on the peer's XFULL barrier with
-// release semantics.  A CTA offers its buffer (arrives on each peer's XRDY
+// CTA writes each peer its unnormalised O^T columns for that peer's heads,
+// read from TMEM and rounded to bf16 pairs of adjacent heads, straight into
+// the peer's chunk buffer (st.shared::cluster; slot `me` of P slots, one
+// 4-byte pair per feature and head pair), together with its (m, l) for those
+// heads, then arrives on the peer's XFULL barrier with release semantics.  A CTA offers its buffer (arrives on each peer's XRDY
 // barrier) once its own last PV product is done.  The receiver merges the
 // pieces:
 //   M = max_r m_r (each m_r starts at the sink),  w_r = 2^(m_r - M),
 //   o = sum_r w_r O_r / (sum_r w_r l_r + 2^(sink*log2e - M))
-// then applies the inverse RoPE when asked and writes its heads.  fp32 keeps
-// the partials' full range and precision whatever the magnitude of kv.
+// then applies the inverse RoPE when asked and writes its heads.  bf16 keeps
+// the partials' full range whatever the magnitude of kv (distributed shared
+// memory moves only ~13 bytes per clock per SM, so the partials go at half
+// the width of fp32); the CTA's own partial stays fp32.
 // Softmax warps only: warp (quarter qd, half hf) handles features
 // 128d + 32qd + lane of tiles d = 2hf, 2hf + 1.  False when a wait ran out.
 
@@ -726,8 +728,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                               int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
 {
     constexpr int HP = H / P;
-    // one piece's O for HP heads: fp32 [HP / 2][512] pairs of heads (2j, 2j + 1) per feature
-    constexpr uint32_t SLOT_BYTES = HP * D * 4;
+    // one piece's O for HP heads: bf16 [HP / 2][512] pairs of heads (2j, 2j + 1) per feature
+    constexpr uint32_t SLOT_BYTES = HP * D * 2;
     static_assert(P * SLOT_BYTES <= KV_BYTES, "receive slots fit the chunk buffer");
     const uint32_t me = cluster_ctarank();
     const uint32_t bar0 = sbase + OFF_BAR;
@@ -735,7 +737,7 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     const float *lt = reinterpret_cast<const float *>(smem + OFF_AUX);   // this piece's row sums
     const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);   // [P][2][HP] peers' (m, l)
     float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights, then [HP] 1/den
-    const float2 *recv = reinterpret_cast<const float2 *>(smem + OFF_KV);   // [P][HP / 2][512]
+    const uint32_t *recv = reinterpret_cast<const uint32_t *>(smem + OFF_KV);   // [P][HP / 2][512] bf16 pairs
     const int fl = 32 * qd + lane;   // feature within a 128-feature tile
 
     if (t < P && t != (int)me)
@@ -770,7 +772,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             }
 #pragma unroll
             for (int i = 0; i < HP; i += 2)
-                st_cluster_v2_b32(dst + (uint32_t)(((i / 2) * D + 128 * d + fl) * 8), v[i], v[i + 1]);
+                st_cluster_b32(dst + (uint32_t)(((i / 2) * D + 128 * d + fl) * 4),
+                               pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
         }
     }
     // every thread's stores are ordered before the arrivals below
@@ -830,9 +833,9 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                 continue;
 #pragma unroll
             for (int i = 0; i < HP; i += 2) {
-                const float2 x = recv[(r * HP + i) / 2 * D + f];
-                o[i] += wts[r * HP + i] * x.x;
-                o[i + 1] += wts[r * HP + i + 1] * x.y;
+                const uint32_t x = recv[(r * HP + i) / 2 * D + f];
+                o[i] += wts[r * HP + i] * bf16lo_to_f32(x);
+                o[i + 1] += wts[r * HP + i + 1] * bf16hi_to_f32(x);
             }
         }
         #pragma unroll

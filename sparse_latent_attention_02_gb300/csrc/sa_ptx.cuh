@@ -133,9 +133,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_v2_b32(uint32_t addr, uint32_t a, uint32_t b)
+__device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t v)
 {
-    asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Orders this thread's earlier memory accesses (including stores into other
