@@ -17,10 +17,14 @@
 // early once that bin is taken whole.  The first pass is folded into the
 // pass that computes the keys, which also finds the last selectable
 // position: the later passes stop there.  The ordered pass gives each warp a
-// contiguous range of positions: the warps count their keys above the
-// threshold and equal to it, and then write, with ballots over 32 positions
-// at a time, every position above it and the first positions equal to it, so
-// that the output is in ascending position order.  Rows of up to CACHE_KEYS
+// contiguous range of positions.  When every key above the threshold is taken
+// and none equal to it (the usual case: only ties leave a share of equal
+// keys), each warp collects its chosen positions in order, with one ballot
+// over 32 positions at a time, in its own segment of the histogram's shared
+// memory, and the segments are written out one after another.  Otherwise the
+// warps first count their keys above the threshold and equal to it, and then
+// write, with ballots, every position above it and the first positions equal
+// to it; either way the output is in ascending position order.  Rows of up to CACHE_KEYS
 // scores keep their keys in shared memory; longer rows are read again from
 // global memory (L2) on every pass.
 #include "sa_internal.h"
@@ -82,6 +86,8 @@ __device__ __forceinline__ int block_scan(int v, int *warp_sums, int &total)
 }
 
 static_assert(THREADS * 8 == BINS, "eight histogram bins per thread");
+// positions a warp can stage in its segment of the histogram's memory (16 bits each)
+constexpr int STAGE_PER_WARP = BINS * 2 / WARPS;   // 512
 
 // CACHED: the row's keys stay in shared memory (L <= CACHE_KEYS)
 template <bool CACHED>
@@ -287,6 +293,46 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
     // multiple of 128 wide; its counts read four consecutive keys a lane
     const int per = ((Lv + WARPS - 1) / WARPS + 127) & ~127;
     const int w0 = min(Lv, warp * per), w1 = min(Lv, w0 + per);
+    const unsigned below = (1u << lane) - 1u;
+    if (CACHED && take_eq == 0 && k <= STAGE_PER_WARP) {
+        // every key above thr is taken, no other (at most k of them): each warp
+        // stages its positions (below CACHE_KEYS: 16 bits) in order in its own
+        // segment of the histogram's memory, which the passes are done with
+        uint16_t *seg = reinterpret_cast<uint16_t *>(hist) + warp * STAGE_PER_WARP;
+        int n = 0;
+        for (int base = w0; base < w1; base += 128) {
+            uint32_t kb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = base + 32 * i + lane;
+                kb[i] = j < w1 ? key_at(j) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool take = kb[i] > thr;
+                const unsigned tm = __ballot_sync(0xffffffffu, take);
+                const int o = n + __popc(tm & below);
+                if (take && o < STAGE_PER_WARP)
+                    seg[o] = (uint16_t)(base + 32 * i + lane);
+                n += __popc(tm);
+            }
+        }
+        if (lane == 0)
+            wcount[0][warp] = n;
+        __syncthreads();
+        int before = 0, all = 0;
+#pragma unroll
+        for (int i = 0; i < WARPS; ++i) {
+            before += i < warp ? wcount[0][i] : 0;
+            all += wcount[0][i];
+        }
+        const int m = min(min(n, STAGE_PER_WARP), max(0, k - before));
+        for (int i = lane; i < m; i += 32)
+            dst[before + i] = (int)seg[i] + offset;
+        for (int i = min(all, k) + t; i < k; i += THREADS)
+            dst[i] = -1;
+        return;
+    }
     // (no key of 0 equals thr: thr is 1 or a selectable key)
     int gt = 0, eq = 0;
     for (int base = w0; base < w1; base += 128) {
@@ -319,7 +365,6 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
     // of all are taken)
     int pos = gt_before + min(eq_before, take_eq);
     int eq_seen = eq_before;
-    const unsigned below = (1u << lane) - 1u;
     for (int base = w0; base < w1; base += 128) {
         uint32_t kb[4];
 #pragma unroll

@@ -369,6 +369,11 @@ def test_block_tail_workload_sampled():
     (24, 1030, 64, "tiny"),       # subnormals, signed zeros and -inf: subnormals are not zero
     (4, 16383, 512, "full"),      # the longest row whose keys stay in shared memory
     (4, 16385, 512, "full"),      # the shortest row read again from L2 on every pass
+    (16, 1024, 512, "cluster"),   # the first pass's bin holds 1024 keys: the most its list takes
+    (16, 1025, 512, "cluster"),   # 1025 keys: every later pass sweeps the whole row
+    (16, 4096, 512, "cluster"),   # scores 1.1 + 1e-4 N(0,1): the low digits decide
+    (16, 4096, 512, "flat"),      # all equal but 10% masked: ties decide every position
+    (8, 20000, 512, "cluster"),   # the same with the keys read again from L2
 ])
 def test_topk_matches_oracle(rows, L, k, mode):
     """The top-k selection is exact: the same int32 positions, in the same
@@ -388,6 +393,11 @@ def test_topk_matches_oracle(rows, L, k, mode):
     elif mode == "tiny":
         vals = torch.tensor([-1e-40, -0.0, 0.0, 1e-45, 1e-40, 2e-40, float("-inf")])
         s = vals[torch.randint(0, len(vals), (rows, L), generator=g)]
+    elif mode == "cluster":
+        s = 1.1 + 1e-4 * s   # one top-digit bin: [1, 1.25)
+    elif mode == "flat":
+        s = torch.ones(rows, L)
+        s[torch.rand(rows, L, generator=g) < 0.1] = float("-inf")
     elif mode == "masked":
         s[torch.rand(rows, L, generator=g) < 0.1] = float("nan")
         s[torch.rand(rows, L, generator=g) < 0.2] = float("-inf")
