@@ -168,7 +168,7 @@ sa_status grouped_gemm(const void *a, const void *w, const float *w_scales, void
     if (!encode_tmap_2d(&g.tm_a, a, (uint64_t)M, (uint64_t)G * Din, 64, 128))
         return SA_ERR_CUDA;
     if (w_scales ? !encode_tmap_2d_u8(&g.tm_b8, w, (uint64_t)G * R, (uint64_t)Din, 64, 128)
-                 : !encode_tmap_2d(&g.tm_b, w, (uint64_t)G * R, (uint64_t)Din, 64, 256))
+                 : !encode_tmap_2d(&g.tm_b, w, (uint64_t)G * R, (uint64_t)Din, 64, 128))
         return SA_ERR_CUDA;
     g.b_scales = w_scales;
     g.y = static_cast<uint16_t *>(y);

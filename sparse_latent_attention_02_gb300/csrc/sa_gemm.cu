@@ -6,22 +6,29 @@
 // product -- G independent GEMMs that share one launch:
 //   y[m, g*R + r] = sum_d o[m, g*Din + d] * W[g*R + r, d]
 //
-// Persistent kernel, one CTA per SM.  Tiles of 128 tokens x 256 rank columns,
-// K in blocks of 64 features.  Warp 0 feeds a 4-stage shared-memory ring with
-// TMA (128-byte swizzle), warp 1 issues tcgen05.mma (M=128, N=256, K=16) into
-// one of two TMEM accumulators, warps 2-5 drain the other accumulator to bf16.
+// bf16 weights (wo_a_pair_kernel): persistent over clusters of two CTAs,
+// one per SM, each pair computing tiles of 256 tokens x 256 rank columns with
+// tcgen05.mma.cta_group::2 (M = 256 split across the pair, N = 256, K = 16),
+// K in blocks of 64 features through a 6-stage TMA ring (128-byte swizzle)
+// in which each CTA holds its own 128 tokens and 128 rank rows; two TMEM
+// accumulators per CTA so that the epilogue of one tile overlaps the main
+// loop of the next.
 //
 // fp8 weights (the page notes that an fp8 grouped GEMM would halve the
 // weight's memory): W is stored as E4M3 with one fp32 scale per 128 x 128
-// block.  Tiles are 256 tokens x 128 rank columns (two M=128 MMAs share each
-// weight block, so every weight is decoded once per 256 tokens), in the same
-// four 48 KB stages.  Warp 14 streams the 128 x 64 blocks of raw E4M3 bytes
-// by TMA into a ring of their own, ahead of the stages; warps 6-13 write each
-// into its stage's swizzled bf16 weight slot as bf16(fp32(value * scale)) --
-// the weight the page's bf16 conversion would give -- as soon as the MMAs
-// have released the slot, while the activations' TMA for the same stage is
-// in flight.  Only the weight's bytes change; the products are the bf16
-// GEMM's.
+// block.  From 512 tokens on, the weight is decoded once into a bf16 copy
+// (dequant_fp8_kernel) and multiplied by the bf16 kernel.  Below that,
+// wo_a_fp8_kernel (one CTA per SM) decodes it on the fly: tiles of 256 tokens
+// x 128 rank columns (two M=128 MMAs share each weight block, so every weight
+// is decoded once per 256 tokens) in four 48 KB stages.  Warp 14 streams the
+// 128 x 64 blocks of raw E4M3 bytes by TMA into a ring of their own, ahead of
+// the stages; warps 6-13 write each into its stage's swizzled bf16 weight
+// slot as bf16(fp32(value * scale)) -- the weight the page's bf16 conversion
+// would give -- as soon as the MMAs have released the slot, while the
+// activations' TMA for the same stage is in flight.  Only the weight's bytes
+// change; the products are the bf16 GEMM's.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,24 +43,24 @@ constexpr int FP8_BLOCK = 128;                // weight rows / columns per fp32 
 constexpr int CONV_WARP0 = 6, CONV_THREADS = 256;
 constexpr int RAW_WARP = CONV_WARP0 + CONV_THREADS / 32;   // 14: TMA of the raw weights
 
-template <bool FP8>
+// The fp8-weight kernel's configuration.
 struct Cfg {
-    static constexpr int BM = FP8 ? 256 : 128;                 // tokens per tile
-    static constexpr int BN = FP8 ? 128 : 256;                 // rank columns per tile
+    static constexpr int BM = 256;                             // tokens per tile
+    static constexpr int BN = 128;                             // rank columns per tile
     static constexpr int HALVES = BM / 128;                    // M=128 MMAs per K step
-    static constexpr uint32_t A_BYTES = BM * BK * 2;           // 16 / 32 KB
-    static constexpr uint32_t B_BYTES = BN * BK * 2;           // 32 / 16 KB
-    static constexpr uint32_t RAW_BYTES = FP8 ? BN * BK : 0;   // raw E4M3 weights of one K block
+    static constexpr uint32_t A_BYTES = BM * BK * 2;           // 32 KB
+    static constexpr uint32_t B_BYTES = BN * BK * 2;           // 16 KB (the decoded weights)
+    static constexpr uint32_t RAW_BYTES = BN * BK;             // raw E4M3 weights of one K block
     static constexpr uint32_t ACC_COLS = HALVES * BN;          // TMEM columns of one accumulator
     static constexpr int STAGES = 4;
-    static constexpr int THREADS = FP8 ? 192 + CONV_THREADS + 32 : 192;
+    static constexpr int THREADS = 192 + CONV_THREADS + 32;
     static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t OFF_RAW = STAGES * STAGE_BYTES;  // raw ring, one slot per stage
     static constexpr uint32_t OFF_BAR = OFF_RAW + STAGES * RAW_BYTES;
     static constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
     static constexpr uint32_t IDESC = idesc_bf16(128, BN, 0, 0);
-    // barriers: TMA full, stage empty, converted (fp8), raw full / free (fp8),
+    // barriers: TMA full, stage empty, converted, raw full / free,
     // accumulators, done
     static constexpr uint32_t B_FULL0 = 0, B_EMPTY0 = STAGES, B_CONV0 = 2 * STAGES, B_RAWFULL0 = 3 * STAGES,
                               B_RAWFREE0 = 4 * STAGES, B_ACCFULL0 = 5 * STAGES, B_ACCEMPTY0 = B_ACCFULL0 + 2,
@@ -61,7 +68,7 @@ struct Cfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(NUM_BARS <= 32, "barrier area");
     static_assert(2 * ACC_COLS <= 512, "two accumulators in TMEM");
-    static_assert(!FP8 || BN % FP8_BLOCK == 0, "a weight tile spans whole scale blocks");
+    static_assert(BN % FP8_BLOCK == 0, "a weight tile spans whole scale blocks");
 };
 
 // Sixteen E4M3 weights times their block's scale, as sixteen bf16 (two
@@ -108,10 +115,9 @@ struct TileMap {
     }
 };
 
-template <bool FP8>
-__global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid_constant__ GemmParams p)
+__global__ void __launch_bounds__(Cfg::THREADS, 1) wo_a_fp8_kernel(const __grid_constant__ GemmParams p)
 {
-    using C = Cfg<FP8>;
+    using C = Cfg;
     constexpr int STAGES = C::STAGES, BM = C::BM, BN = C::BN;
     constexpr uint32_t STAGE_BYTES = C::STAGE_BYTES, OFF_BAR = C::OFF_BAR, OFF_MISC = C::OFF_MISC;
     constexpr uint32_t A_BYTES = C::A_BYTES;
@@ -149,7 +155,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tm_a);
-        prefetch_tmap(FP8 ? &p.tm_b8 : &p.tm_b);
+        prefetch_tmap(&p.tm_b8);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -176,13 +182,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
                     }
                     const uint32_t fb = bar0 + 8 * (B_FULL0 + stage);
                     const uint32_t sa_ = sbase + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(fb, A_BYTES + (FP8 ? 0u : C::B_BYTES));
+                    mbar_arrive_expect_tx(fb, A_BYTES);
                     // activations: 128-row boxes (rows past M read as zero)
 #pragma unroll
                     for (int h = 0; h < C::HALVES; ++h)
                         tma_load_2d(sa_ + h * 128 * BK * 2, &p.tm_a, g * p.Din + kb * BK, mb * BM + 128 * h, fb);
-                    if (!FP8)
-                        tma_load_2d(sa_ + A_BYTES, &p.tm_b, kb * BK, g * p.R + nb * BN, fb);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -218,9 +222,9 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
                 tc_fence_after();
                 const uint32_t dt = tmem + (uint32_t)(a * C::ACC_COLS);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    // the stage's TMA has landed; fp8: the converters are done too
+                    // the stage's TMA has landed and the converters are done
                     if (!bounded_wait(bar0 + 8 * (B_FULL0 + stage), ph, abort_flag, p.timeout_ns) ||
-                        (FP8 && !bounded_wait(bar0 + 8 * (B_CONV0 + stage), ph, abort_flag, p.timeout_ns))) {
+                        !bounded_wait(bar0 + 8 * (B_CONV0 + stage), ph, abort_flag, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
                     break;
         }
         __syncwarp();
-    } else if (FP8 && warp == RAW_WARP) {
+    } else if (warp == RAW_WARP) {
         // ---------------- TMA of the raw E4M3 weight blocks into their ring
         if (lane == 0) {
             uint32_t slot = 0, ph = 0, issued = 0;
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
             }
         }
         __syncwarp();
-    } else if (FP8 && warp >= CONV_WARP0) {
+    } else if (warp >= CONV_WARP0) {
         // ---------------- fp8 weights -> swizzled bf16 operand (warps 6..13).
         // Thread ct converts 16-byte pieces i = ct + 256 it of the raw BN x 64
         // block (row i / 4, piece i % 4 = features 16 (i % 4) ..); the block lies
@@ -390,6 +394,236 @@ __global__ void __launch_bounds__(Cfg<FP8>::THREADS, 1) wo_a_kernel(const __grid
     }
 }
 
+// ---------------------------------------------------------------- two-SM bf16 GEMM
+//
+// bf16 weights: a cluster of two CTAs (one per SM) computes tiles of 256
+// tokens x 256 rank columns with tcgen05.mma.cta_group::2 (M = 256 across
+// the pair, N = 256, K = 16), issued by the even CTA.  Per 64-wide K block
+// each CTA's stage holds its 128 tokens of A and its 128 rank rows of B
+// (32 KB), so each SM's shared memory takes 32 KB of TMA writes and serves
+// 32 KB of operand reads per 512 MMA cycles -- about the 128 bytes per clock
+// it can move -- where one SM alone with N = 256 needs 48 KB of each.
+//   warp 0 (both CTAs): TMA producer; each stage's two loads complete their
+//     bytes on the even CTA's full barrier (two arrivals: one per CTA)
+//   warp 1: TMEM owner (both CTAs, collective pair allocation) and, in the
+//     even CTA, the MMA issuer; its commits arrive on both CTAs' barriers
+//   warps 2-5 (both CTAs): epilogue from their own TMEM (tile rows 128 r ..,
+//     r = rank), releasing the accumulator on the even CTA's barrier
+namespace pair {
+
+constexpr int BM = 256, BN = 256, STAGES = 6, THREADS = 192;
+constexpr uint32_t A_BYTES = 128 * BK * 2;        // this CTA's 128 tokens x 64 features
+constexpr uint32_t B_BYTES = 128 * BK * 2;        // this CTA's 128 rank rows x 64 features
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;
+constexpr uint32_t OFF_MISC = OFF_BAR + 32 * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+constexpr uint32_t ACC_COLS = BN;                  // one accumulator: 256 TMEM columns
+constexpr uint32_t IDESC = idesc_bf16(256, BN, 0, 0);
+// barriers: full (even CTA: both CTAs' loads), empty (each CTA), accumulator
+// full (each CTA) / empty (even CTA: both CTAs' epilogues), done (even CTA)
+constexpr uint32_t B_FULL0 = 0, B_EMPTY0 = STAGES, B_ACCFULL0 = 2 * STAGES, B_ACCEMPTY0 = B_ACCFULL0 + 2,
+                   B_DONE = B_ACCEMPTY0 + 2, NUM_BARS = B_DONE + 1;
+constexpr uint32_t EPI_WARPS = 4;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(NUM_BARS <= 32, "barrier area");
+static_assert(2 * ACC_COLS <= 512, "two accumulators in TMEM");
+
+__global__ void __launch_bounds__(THREADS, 1) wo_a_pair_kernel(const __grid_constant__ GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + OFF_BAR;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+    // the even CTA's barriers, as cluster addresses
+    const uint32_t lead0 = mapa_shared(bar0, 0);
+
+    TileMap tm;
+    tm.num_m = (p.M + BM - 1) / BM;
+    tm.num_n = p.R / BN;
+    tm.total = tm.num_m * tm.num_n * p.G;
+    const int kblocks = p.Din / BK;
+    const int pair_id = (int)(blockIdx.x >> 1), num_pairs = (int)(gridDim.x >> 1);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar0 + 8 * (B_FULL0 + s), 2);
+            mbar_init(bar0 + 8 * (B_EMPTY0 + s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar0 + 8 * (B_ACCFULL0 + a), 1);
+            mbar_init(bar0 + 8 * (B_ACCEMPTY0 + a), 2 * EPI_WARPS);
+        }
+        mbar_init(bar0 + 8 * B_DONE, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&p.tm_a);
+        prefetch_tmap(&p.tm_b);
+    }
+    if (warp == 1)
+        tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers are initialised before either arrives on the other's
+    __syncwarp();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t stage = 0, ph = 0, issued = 0;
+            bool ok = true;
+            for (int id = pair_id; id < tm.total && ok; id += num_pairs) {
+                int g, mb, nb;
+                tm.at(id, g, mb, nb);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!bounded_wait(bar0 + 8 * (B_EMPTY0 + stage), ph ^ 1u, abort_flag, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = lead0 + 8 * (B_FULL0 + stage);
+                    const uint32_t sa_ = sbase + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx_cluster(fb, STAGE_BYTES);
+                    // this CTA's 128 tokens (rows past M read as zero) and 128 rank rows
+                    tma_load_2d_pair(sa_, &p.tm_a, g * p.Din + kb * BK, mb * BM + 128 * (int)rank, fb);
+                    tma_load_2d_pair(sa_ + A_BYTES, &p.tm_b, kb * BK, g * p.R + nb * BN + 128 * (int)rank, fb);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // the even CTA sees every load land (its full barriers count both
+            // CTAs' bytes) before the pair may leave: load n went to stage
+            // n % STAGES, phase (n / STAGES) & 1
+            if (rank == 0) {
+                for (uint32_t k = 0; k < STAGES && k < issued; ++k) {
+                    const uint32_t n = issued - 1 - k;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(bar0 + 8 * (B_FULL0 + n % STAGES), (n / STAGES) & 1u))
+                        if (globaltimer_ns() - t0 > p.timeout_ns)
+                            break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (even CTA)
+        if (rank == 0 && lane == 0) {
+            uint32_t stage = 0, ph = 0;
+            uint32_t acc_ph[2] = {0, 0};
+            int local = 0;
+            bool ok = true;
+            for (int id = pair_id; id < tm.total && ok; id += num_pairs, ++local) {
+                const int a = local & 1;
+                // both CTAs' epilogues have drained this accumulator
+                if (!bounded_wait(bar0 + 8 * (B_ACCEMPTY0 + a), acc_ph[a] ^ 1u, abort_flag, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                acc_ph[a] ^= 1u;
+                tc_fence_after();
+                const uint32_t dt = tmem + (uint32_t)(a * ACC_COLS);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    // both CTAs' loads of the stage have landed
+                    if (!bounded_wait(bar0 + 8 * (B_FULL0 + stage), ph, abort_flag, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa_ = sbase + stage * STAGE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = smem_desc_sw128(sa_ + k * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(sa_ + A_BYTES + k * 32, 16, 1024);
+                        mma_bf16_ss_pair(dt, ad, bd, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    // the stage is free in both CTAs once these products complete
+                    mma_commit_pair(bar0 + 8 * (B_EMPTY0 + stage), 3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (ok)
+                    mma_commit_pair(bar0 + 8 * (B_ACCFULL0 + a), 3);
+            }
+            mma_commit_pair(bar0 + 8 * B_DONE, 1);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar0 + 8 * B_DONE, 0))
+                if (globaltimer_ns() - t0 > p.timeout_ns)
+                    break;
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2..5 -> TMEM lane quarters 2,3,0,1
+        // (tile rows 128 rank + 32 quarter + lane)
+        const int quarter = warp & 3;
+        const int row = 128 * (int)rank + quarter * 32 + lane;
+        uint32_t acc_ph[2] = {0, 0};
+        int local = 0;
+        for (int id = pair_id; id < tm.total; id += num_pairs, ++local) {
+            const int a = local & 1;
+            int ok = 0;
+            if (lane == 0)
+                ok = bounded_wait(bar0 + 8 * (B_ACCFULL0 + a), acc_ph[a], abort_flag, p.timeout_ns) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            acc_ph[a] ^= 1u;
+            if (bar_red_or(1, 32 * EPI_WARPS, ok == 0))
+                break;
+            tc_fence_after();
+            int g, mb, nb;
+            tm.at(id, g, mb, nb);
+            const int m = mb * BM + row;
+            const uint32_t ta = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(a * ACC_COLS);
+            uint16_t *yrow = p.y + (size_t)m * (p.G * p.R) + g * p.R + nb * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(ta + 32 * c, v);
+                tmem_wait_ld();
+                if (m < p.M) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * c);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(
+                            pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1])),
+                            pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                            pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                            pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(lead0 + 8 * (B_ACCEMPTY0 + a));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA releases its tensor memory or leaves while the pair's
+    // products, loads or arrivals may still touch it
+    __syncwarp();
+    cluster_sync();
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicOr(p.err, ERRBIT_TIMEOUT);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
+}  // namespace pair
+
 // E4M3 weight [rows, cols] with one fp32 scale per 128 x 128 block -> bf16
 // [rows, cols], each value bf16(fp32(e4m3 * scale)) as in the fused decoders;
 // a thread converts 16 bytes per step (grid-stride).  cols % 128 == 0.
@@ -431,19 +665,59 @@ cudaError_t launch_dequant_fp8(const uint8_t *w8, const float *scales, uint16_t 
 cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st)
 {
     const bool fp8 = p.b_scales != nullptr;
-    void (*kernel)(GemmParams) = fp8 ? gemm::wo_a_kernel<true> : gemm::wo_a_kernel<false>;
-    const int smem = (int)(fp8 ? gemm::Cfg<true>::SMEM_BYTES : gemm::Cfg<false>::SMEM_BYTES);
-    const int threads = fp8 ? gemm::Cfg<true>::THREADS : gemm::Cfg<false>::THREADS;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (!fp8) {
+        // bf16 weights: the two-SM kernel, persistent over as many clusters of
+        // two CTAs as can be resident at once (a cluster needs both SMs in one
+        // GPC, so that is fewer than half the SMs: a grid of half the SMs
+        // would leave a second wave)
+        cudaError_t e = cudaFuncSetAttribute(gemm::pair::wo_a_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)gemm::pair::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return e;
+        const int tiles = ((p.M + gemm::pair::BM - 1) / gemm::pair::BM) * (p.R / gemm::pair::BN) * p.G;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(gemm::pair::THREADS);
+        cfg.dynamicSmemBytes = gemm::pair::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // resident clusters: asked once per device (a host query, nothing enqueued)
+        static std::atomic<int> resident_of[64];
+        int dev = 0;
+        e = cudaGetDevice(&dev);
+        if (e != cudaSuccess)
+            return e;
+        int resident = dev < 64 ? resident_of[dev].load() : 0;
+        if (resident <= 0) {
+            cfg.gridDim = dim3((unsigned)(num_sms / 2 * 2));
+            e = cudaOccupancyMaxActiveClusters(&resident, gemm::pair::wo_a_pair_kernel, &cfg);
+            if (e != cudaSuccess)
+                return e;
+            if (dev < 64)
+                resident_of[dev].store(resident);
+        }
+        int pairs = tiles < resident ? tiles : resident;
+        if (pairs <= 0)
+            return tiles <= 0 ? cudaSuccess : cudaErrorLaunchOutOfResources;
+        cfg.gridDim = dim3((unsigned)(2 * pairs));
+        return cudaLaunchKernelEx(&cfg, gemm::pair::wo_a_pair_kernel, p);
+    }
+    // fp8 weights decoded inside the kernel (fewer than 512 tokens)
+    using C = gemm::Cfg;
+    cudaError_t e = cudaFuncSetAttribute(gemm::wo_a_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    const int bm = fp8 ? gemm::Cfg<true>::BM : gemm::Cfg<false>::BM;
-    const int bn = fp8 ? gemm::Cfg<true>::BN : gemm::Cfg<false>::BN;
-    const int tiles = ((p.M + bm - 1) / bm) * (p.R / bn) * p.G;
+    const int tiles = ((p.M + C::BM - 1) / C::BM) * (p.R / C::BN) * p.G;
     const int grid = tiles < num_sms ? tiles : num_sms;
     if (grid <= 0)
         return cudaSuccess;
-    kernel<<<grid, threads, smem, st>>>(p);
+    gemm::wo_a_fp8_kernel<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p);
     return cudaGetLastError();
 }
 

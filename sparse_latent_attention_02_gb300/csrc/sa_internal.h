@@ -66,7 +66,7 @@ cudaError_t launch_attention(AttnParams &p, const Schedule &s, cudaStream_t st);
 
 struct GemmParams {
     CUtensorMap tm_a;          // o as 2-D [M rows, G*Din cols] bf16, box 64x128
-    CUtensorMap tm_b;          // W as 2-D [G*R rows, Din cols] bf16, box 64x256
+    CUtensorMap tm_b;          // W as 2-D [G*R rows, Din cols] bf16, box 64x128 (one CTA's half of a tile)
     CUtensorMap tm_b8;         // fp8 W: E4M3 bytes [G*R rows, Din cols], box 64x128, no swizzle
     const float *b_scales;     // fp8 W: fp32 [G*R/128, Din/128] block scales; null for bf16 W
     uint16_t *y;               // bf16 [M, G*R]
