@@ -43,14 +43,27 @@ from sparse_latent_attention_02_gb300 import inputs as I  # noqa: E402
 METRIC = "sparse_attn queries/s; decode gathered-KV GB/s & prefill TFLOP/s vs GB300 roofline"
 HEADLINE = "decode"
 
-# DRAM bytes (read + write) per launch of the attention kernel, from one ncu capture
-# of the workload (the commands are in profiles/), keyed by the SHA-256 of the kernel
-# source they were taken on: a changed kernel reports null until it is captured again.
-KERNEL_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)),
-                          "sparse_latent_attention_02_gb300", "csrc", "sa_attn.cu")
+# DRAM bytes (read + write) per call -- every kernel the call launches -- from one
+# ncu capture of the workload (the commands are in profiles/), keyed by the SHA-256
+# of the kernel sources the call runs: a changed kernel reports null until it is
+# captured again.  The long-decode figure was captured with 8192 compressed rows per
+# batch row instead of 65536 (the same 640-entry lists, each query gathering from
+# its own batch row, so the same rows move per call).
+CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_latent_attention_02_gb300", "csrc")
+KERNEL_SRC = os.path.join(CSRC, "sa_attn.cu")
+GEMM_SRC = os.path.join(CSRC, "sa_gemm.cu")
+TOPK_SRC = os.path.join(CSRC, "sa_topk.cu")
+TRAFFIC_SOURCES = {
+    "decode": ("attn",), "long_decode": ("attn",), "prefill": ("attn",),
+    "fused_tail": ("attn", "gemm"), "block_tail": ("attn", "gemm"), "topk": ("topk",),
+}
 MEASURED_TRAFFIC = {
-    "decode": ("f093ba96370f5f0dbb91c54c752a0635227b629290b4d88e9bbcb3bb73438a98", 46_795_520),
-    "prefill": ("f093ba96370f5f0dbb91c54c752a0635227b629290b4d88e9bbcb3bb73438a98", 1_056_809_472),
+    "decode": ("ddf55976e5db3b9c81be0df0c9674d55036c8c3320ec778298792f91925c115c", 46_608_242),
+    "long_decode": ("ddf55976e5db3b9c81be0df0c9674d55036c8c3320ec778298792f91925c115c", 87_614_094),
+    "prefill": ("ddf55976e5db3b9c81be0df0c9674d55036c8c3320ec778298792f91925c115c", 1_054_894_304),
+    "fused_tail": ("9236abb7ff8dcca53bd47864f5d9c2c04436eec6b46194ad95a0fa705461136a", 1_792_871_776),
+    "block_tail": ("9236abb7ff8dcca53bd47864f5d9c2c04436eec6b46194ad95a0fa705461136a", 2_781_783_552),
+    "topk": ("8bee89868215d32e69245f02aef9a050199e46091e6e3bd6673116ad24b2aa48", 139_249_010),
 }
 
 
@@ -59,9 +72,12 @@ def measured_traffic(workload):
     entry = MEASURED_TRAFFIC.get(workload)
     if entry is None:
         return None
-    with open(KERNEL_SRC, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    return entry[1] if digest == entry[0] else None
+    paths = {"attn": KERNEL_SRC, "gemm": GEMM_SRC, "topk": TOPK_SRC}
+    digest = hashlib.sha256()
+    for key in TRAFFIC_SOURCES[workload]:
+        with open(paths[key], "rb") as f:
+            digest.update(f.read())
+    return entry[1] if digest.hexdigest() == entry[0] else None
 
 
 # ------------------------------------------------------------------ algorithmic work
@@ -288,9 +304,10 @@ def launches_per_call(wl: I.Workload, num_sms: int) -> int:
     return 1 + (1 if wl.tail else 0) + (1 if wl.wo_b else 0)
 
 
-def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_sets=None, cpu_s: float = 0.0):
+def bench_workload(name: str, steps: int, warmup: int, dev, with_e2e: bool, n_sets=None, cpu_s: float = 0.0,
+                   wl: I.Workload = None):
     import sparse_latent_attention_02_gb300 as sa
-    wl = I.WORKLOADS[name]
+    wl = I.WORKLOADS[name] if wl is None else wl
     sets = sets_for(wl, dev, n_sets=n_sets)
     outs = []
     fns = []
@@ -441,7 +458,7 @@ def bench_topk(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 0.0) -> di
     gbs = nbytes / step_s / 1e9
     res = {"ms_per_step": step_s * 1e3, "rows_per_s": rows / step_s, "bytes_per_step": nbytes,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / pk["hbm_gbs"], "traffic": None}}
+                        "frac": gbs / pk["hbm_gbs"], "traffic": measured_traffic("topk")}}
     if cpu_s > 0:
         import oracle
         n = 256
@@ -656,8 +673,11 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
+    head_wl = I.WORKLOADS[args.workload]
+    if args.kv_rows is not None:   # profiling aid: a smaller compressed cache, the same lists' shape
+        head_wl = I.scaled(head_wl, C=args.kv_rows)
     head = bench_workload(args.workload, args.steps, args.warmup, dev,
-                          with_e2e=not args.no_e2e and world == 1, n_sets=args.sets, cpu_s=cpu_s)
+                          with_e2e=not args.no_e2e and world == 1, n_sets=args.sets, cpu_s=cpu_s, wl=head_wl)
     secs, units = aggregate_over_ranks(head["ms_per_step"] * 1e-3 * args.steps,
                                        head["queries_per_s"] * head["ms_per_step"] * 1e-3 * args.steps)
     head["job_queries_per_s"] = units / secs
@@ -756,11 +776,16 @@ def main():
     ap.add_argument("--sets", type=int, default=None,
                     help="number of rotating input sets (default: enough for > 2x L2)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--kv-rows", type=int, default=None,
+                    help="profiling aid: compressed rows per batch row of the headline workload "
+                         "(the lists keep their length; only with --headline-only)")
     ap.add_argument("--extra", choices=sorted(EXTRA_LINES),
                     help="time only this additional line (one GPU) and print it as JSON")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.kv_rows is not None and (not args.headline_only or args.kv_rows < 1):
+        ap.error("--kv-rows takes a positive count and --headline-only")
     if args.extra:
         import sparse_latent_attention_02_gb300 as sa
         sa.build()

@@ -43,6 +43,15 @@ def test_traffic_table_is_keyed_to_the_kernel_source(tmp_path, monkeypatch):
     """A measured traffic figure is reported only for the kernel source it was
     captured on."""
     assert bench.measured_traffic("no such workload") is None
+    for w in bench.MEASURED_TRAFFIC:
+        assert w in bench.TRAFFIC_SOURCES
+    if bench.measured_traffic("fused_tail") is not None and bench.measured_traffic("decode") is not None:
+        # a changed GEMM drops the tails' figures, not the attention-only ones
+        changed = tmp_path / "sa_gemm.cu"
+        changed.write_text(open(bench.GEMM_SRC).read() + "\n// changed\n")
+        monkeypatch.setattr(bench, "GEMM_SRC", str(changed))
+        assert bench.measured_traffic("fused_tail") is None
+        assert bench.measured_traffic("decode") is not None
     if bench.measured_traffic("decode") is not None:
         changed = tmp_path / "sa_attn.cu"
         changed.write_text(open(bench.KERNEL_SRC).read() + "\n// changed\n")
