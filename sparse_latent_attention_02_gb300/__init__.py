@@ -495,5 +495,10 @@ def rope_table(theta: float, start_pos: int, T: int, rope_dim: int = 64) -> torc
 
 
 def check_errors(workspace: torch.Tensor, stream=None):
-    """Synchronise, read and clear the workspace error word; raise SAError if set."""
+    """Synchronise, read and clear the workspace error word; raise SAError if set.
+
+    A device-detected error (an index outside [-1, N), a wait that ran out)
+    stays OR-ed into the workspace's error word across later calls on the same
+    workspace until this function reads and clears it: a clean call does not
+    clear an earlier call's error."""
     _check(library().sa_check_errors(workspace.data_ptr(), _stream_ptr(stream)), "device")
