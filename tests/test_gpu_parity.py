@@ -527,6 +527,36 @@ def test_fused_tail_fp8_matches_dequantized_weight(B, T, K, N, G, R):
             yref.reshape(len(qs), -1), f"fp8 tail G{G}")
 
 
+@pytest.mark.parametrize("M", [1, 127, 128, 129, 255, 256, 257, 520])
+def test_tails_at_pair_tile_edges(M):
+    """The bf16 GEMMs run on CTA pairs, each pair a tile of 256 tokens (128
+    per CTA): token counts on both sides of 128 and 256, and below 128 where
+    the second CTA of the pair holds no token.  Every row of the fused tail
+    (G = 8, R = 256) and of a block tail (then wo_b to 512 features) against
+    the fp64 chain of oracle steps."""
+    g = torch.Generator().manual_seed(7000 + M)
+    B, T, K, N, G, R, dim = 1, M, 64, 100, 8, 256, 512
+    q = torch.randn(B, T, 64, 512, generator=g).to(torch.bfloat16)
+    kv = I.rms_rows(torch.randn(B, N, 512, generator=g)).to(torch.bfloat16)
+    sink = torch.randn(64, generator=g)
+    idx = torch.randint(0, N, (B, T, K), generator=g, dtype=torch.int32)
+    idx[torch.rand(B, T, K, generator=g) < 0.1] = -1
+    wa = (0.02 * torch.randn(G, R, 64 * 512 // G, generator=g)).to(torch.bfloat16)
+    wb = (0.02 * torch.randn(dim, G * R, generator=g)).to(torch.bfloat16)
+    rope = sa.rope_table(160000.0, 0, T, 64).cuda()
+    x = to_dev(dict(q=q, kv=kv, sink=sink, idx=idx))
+    y = sa.sparse_attn_rope_wo_a(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5, rope, wa.cuda(), check=True)
+    z = sa.sparse_attn_block_tail(x["q"], x["kv"], x["sink"], x["idx"], 512 ** -0.5, rope, wa.cuda(), wb.cuda(),
+                                  check=True)
+    qs = np.arange(B * T)
+    o = oracle_rows(dict(q=q, kv=kv, sink=sink, idx=idx), qs, 512 ** -0.5)
+    o = oracle.inverse_rope(o, qs % T, 64, 160000.0)
+    yref = oracle.wo_a(o.reshape(len(qs), G, -1), wa)
+    compare(y.reshape(-1, G * R).double().cpu().numpy(), yref.reshape(len(qs), -1), f"fused tail M{M}")
+    zref = oracle.wo_b(yref.reshape(len(qs), -1), wb)
+    compare(z.reshape(-1, dim).double().cpu().numpy(), zref, f"block tail M{M}", per_value=True)
+
+
 def test_fused_calls_on_two_streams_keep_their_own_workspace():
     """Fused calls in flight on two streams at once, each with the binding's
     default workspace (where the attention output waits for the GEMM), give
