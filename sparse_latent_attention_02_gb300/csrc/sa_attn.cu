@@ -724,8 +724,9 @@ __device__ __forceinline__ void store_bf16_pairs(uint16_t *out_h0, int f, const 
 }
 
 template <int P>
-__device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl, const Seg &s,
-                              int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
+__device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl,
+                                              const Seg &s, int nc, int t, int qd, int hf, volatile int *abort_flag,
+                                              int lane)
 {
     constexpr int HP = H / P;
     // one piece's O for HP heads: bf16 [HP / 2][512] pairs of heads (2j, 2j + 1) per feature
@@ -736,12 +737,12 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     const float *m_s = reinterpret_cast<const float *>(smem + OFF_M);
     const float *lt = reinterpret_cast<const float *>(smem + OFF_AUX);   // this piece's row sums
     const float *xst = reinterpret_cast<const float *>(smem + OFF_XSTAT);   // [P][2][HP] peers' (m, l)
-    float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights, then [HP] 1/den
+    float *wts = reinterpret_cast<float *>(smem + OFF_RED);   // [P][HP] weights w_r / den
     const uint32_t *recv = reinterpret_cast<const uint32_t *>(smem + OFF_KV);   // [P][HP / 2][512] bf16 pairs
     const int fl = 32 * qd + lane;   // feature within a 128-feature tile
 
-    if (t < P && t != (int)me)
-        mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
+    // (this CTA offered its buffer on each peer's XRDY barrier as soon as its
+    // last PV product was done)
     bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
     if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
         return false;
@@ -794,17 +795,20 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
         for (int r = 0; r < P; ++r)
             if (r != (int)me)
                 M = fmaxf(M, xst[r * 2 * HP + t]);
+        float w[P];
         float den = 0.f;
 #pragma unroll
         for (int r = 0; r < P; ++r) {
             const float mr = r == (int)me ? m_s[h] : xst[r * 2 * HP + t];
             const float lr = r == (int)me ? lt[h] : xst[r * 2 * HP + HP + t];
-            const float w = M == -INFINITY ? 0.f : ex2(mr - M);
-            wts[r * HP + t] = w;
-            den += w * lr;
+            w[r] = M == -INFINITY ? 0.f : ex2(mr - M);
+            den += w[r] * lr;
         }
         den += M == -INFINITY ? 0.f : ex2(sl - M);
-        wts[P * HP + t] = den > 0.f ? 1.f / den : 0.f;
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+        for (int r = 0; r < P; ++r)
+            wts[r * HP + t] = w[r] * inv;
     }
     bar_sync(1, SMX_THREADS);
 
@@ -823,24 +827,33 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             for (int i = 0; i < HP; ++i)
                 v[i] = 0u;
         }
+        // weights read four heads at a time (16-byte shared loads, the same
+        // address in every lane)
+        const float4 *w4 = reinterpret_cast<const float4 *>(wts);
         float o[HP];
 #pragma unroll
-        for (int i = 0; i < HP; ++i)
-            o[i] = wts[me * HP + i] * __uint_as_float(v[i]);
+        for (int i = 0; i < HP; i += 4) {
+            const float4 a = w4[(me * HP + i) / 4];
+            o[i] = a.x * __uint_as_float(v[i]);
+            o[i + 1] = a.y * __uint_as_float(v[i + 1]);
+            o[i + 2] = a.z * __uint_as_float(v[i + 2]);
+            o[i + 3] = a.w * __uint_as_float(v[i + 3]);
+        }
 #pragma unroll
         for (int r = 0; r < P; ++r) {
             if (r == (int)me)
                 continue;
 #pragma unroll
-            for (int i = 0; i < HP; i += 2) {
-                const uint32_t x = recv[(r * HP + i) / 2 * D + f];
-                o[i] += wts[r * HP + i] * bf16lo_to_f32(x);
-                o[i + 1] += wts[r * HP + i + 1] * bf16hi_to_f32(x);
+            for (int i = 0; i < HP; i += 4) {
+                const float4 a = w4[(r * HP + i) / 4];
+                const uint32_t x0 = recv[(r * HP + i) / 2 * D + f];
+                const uint32_t x1 = recv[((r * HP + i) / 2 + 1) * D + f];
+                o[i] += a.x * bf16lo_to_f32(x0);
+                o[i + 1] += a.y * bf16hi_to_f32(x0);
+                o[i + 2] += a.z * bf16lo_to_f32(x1);
+                o[i + 3] += a.w * bf16hi_to_f32(x1);
             }
         }
-        #pragma unroll
-        for (int i = 0; i < HP; ++i)
-            o[i] *= wts[P * HP + i];
         if (p.rope_dim > 0 && f >= D - p.rope_dim) {   // warp-uniform
             const int pi = (f - (D - p.rope_dim)) >> 1;
             const float *cs = p.rope + ((size_t)(s.q % p.T) * (p.rope_dim >> 1) + pi) * 2;
@@ -1010,6 +1023,10 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                 break;
             tc_fence_after();
         }
+        // split schedule: the chunk buffer is free; offer it to the peers now,
+        // ahead of the row sums (they write their partials into it)
+        if (!s.full && t < p.pieces && t != (int)cluster_ctarank())
+            mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XRDY, (uint32_t)t));
 
         // row sums: reduce the per-row partials over the rows of each warp, then the quarters
         red[qd * 64 + hb + lane] = warp_reduce32<false>(l, lane);
