@@ -285,11 +285,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_a
                  : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Fire-and-forget L2 prefetch of the 128-byte line holding addr.
 __device__ __forceinline__ void prefetch_l2_line(const void *addr)
 {
