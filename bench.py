@@ -56,14 +56,17 @@ TOPK_SRC = os.path.join(CSRC, "sa_topk.cu")
 TRAFFIC_SOURCES = {
     "decode": ("attn",), "long_decode": ("attn",), "prefill": ("attn",),
     "fused_tail": ("attn", "gemm"), "block_tail": ("attn", "gemm"), "topk": ("topk",),
+    "decode_fp4": ("attn",), "fused_tail_fp8": ("attn", "gemm"),
 }
 MEASURED_TRAFFIC = {
-    "decode": ("ddf55976e5db3b9c81be0df0c9674d55036c8c3320ec778298792f91925c115c", 46_608_242),
-    "long_decode": ("ddf55976e5db3b9c81be0df0c9674d55036c8c3320ec778298792f91925c115c", 87_614_094),
-    "prefill": ("ddf55976e5db3b9c81be0df0c9674d55036c8c3320ec778298792f91925c115c", 1_054_894_304),
-    "fused_tail": ("9236abb7ff8dcca53bd47864f5d9c2c04436eec6b46194ad95a0fa705461136a", 1_792_871_776),
-    "block_tail": ("9236abb7ff8dcca53bd47864f5d9c2c04436eec6b46194ad95a0fa705461136a", 2_781_783_552),
+    "decode": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 46_876_188),
+    "long_decode": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 87_940_807),
+    "prefill": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 1_055_243_040),
+    "fused_tail": ("fccab286eb25f06cf57fc0003945371c2ee4d7ad20dbfdb1f9d11bfe4df3cfcf", 1_794_871_232),
+    "block_tail": ("fccab286eb25f06cf57fc0003945371c2ee4d7ad20dbfdb1f9d11bfe4df3cfcf", 2_784_149_248),
     "topk": ("8bee89868215d32e69245f02aef9a050199e46091e6e3bd6673116ad24b2aa48", 139_249_010),
+    "decode_fp4": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 25_182_643),
+    "fused_tail_fp8": ("fccab286eb25f06cf57fc0003945371c2ee4d7ad20dbfdb1f9d11bfe4df3cfcf", 1_835_902_592),
 }
 
 
@@ -508,7 +511,7 @@ def bench_decode_fp4(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 0.0)
     gbs = nbytes / step_s / 1e9
     res = {"ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "bytes_per_step": nbytes,
            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / pk["hbm_gbs"], "traffic": None}}
+                        "frac": gbs / pk["hbm_gbs"], "traffic": measured_traffic("decode_fp4")}}
     if cpu_s > 0:
         import oracle
         x, win, c, sc = sets[0][:4]
@@ -555,7 +558,7 @@ def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 
     res = {"ms_per_step": step_s * 1e3, "queries_per_s": wl.n_queries / step_s, "flops_per_step": int(flops),
            "gpu_launches": 3 * steps,
            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                        "frac": tflops / peak, "traffic": None, "peak_note": note}}
+                        "frac": tflops / peak, "traffic": measured_traffic("fused_tail_fp8"), "peak_note": note}}
     if cpu_s > 0:
         import oracle
         x = dict(sets[0])
