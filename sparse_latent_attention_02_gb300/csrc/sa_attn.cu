@@ -685,14 +685,16 @@ __device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity,
 }
 
 // Split schedule: the P pieces of one query's list run as one cluster, and
-// CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  Every
-// CTA writes each peer its unnormalised O^T columns for that peer's heads,
-// read from TMEM and rounded to bf16 pairs of adjacent heads, straight into
-// the peer's chunk buffer (st.shared::cluster; slot `me` of P slots, one
-// 4-byte pair per feature and head pair), together with its (m, l) for those
-// heads, then arrives on the peer's XFULL barrier with release semantics.  A CTA offers its buffer (arrives on each peer's XRDY
-// barrier) once its own last PV product is done.  The receiver merges the
-// pieces:
+// CTA r of the cluster finishes heads [r*HP, (r+1)*HP), HP = 64 / P.  A CTA
+// offers its chunk buffer (arrives on each peer's XRDY barrier) once its own
+// last PV product is done.  Once all its peers have offered theirs, every CTA
+// writes each peer its unnormalised O^T columns for that peer's heads, read
+// from TMEM and rounded to bf16 pairs of adjacent heads, straight into the
+// peer's chunk buffer (slot `me` of P slots, one 4-byte pair per feature and
+// head pair), together with its (m, l) for those heads, by asynchronous
+// stores (st.async) whose bytes complete on the peer's XFULL barrier; each
+// CTA armed its own XFULL barrier with the bytes it expects.  The receiver
+// merges the pieces:
 //   M = max_r m_r (each m_r starts at the sink),  w_r = 2^(m_r - M),
 //   o = sum_r w_r O_r / (sum_r w_r l_r + 2^(sink*log2e - M))
 // then applies the inverse RoPE when asked and writes its heads.  bf16 keeps
@@ -724,9 +726,8 @@ __device__ __forceinline__ void store_bf16_pairs(uint16_t *out_h0, int f, const 
 }
 
 template <int P>
-__device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl,
-                                              const Seg &s, int nc, int t, int qd, int hf, volatile int *abort_flag,
-                                              int lane)
+__device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase, uint32_t tl, const Seg &s,
+                              int nc, int t, int qd, int hf, volatile int *abort_flag, int lane)
 {
     constexpr int HP = H / P;
     // one piece's O for HP heads: bf16 [HP / 2][512] pairs of heads (2j, 2j + 1) per feature
@@ -741,6 +742,9 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     const uint32_t *recv = reinterpret_cast<const uint32_t *>(smem + OFF_KV);   // [P][HP / 2][512] bf16 pairs
     const int fl = 32 * qd + lane;   // feature within a 128-feature tile
 
+    // every peer's partial and (m, l) land on this CTA's XFULL barrier as bytes
+    if (t == 0)
+        mbar_arrive_expect_tx(bar0 + 8 * B_XFULL, (uint32_t)(P - 1) * (SLOT_BYTES + 2 * HP * 4));
     // (this CTA offered its buffer on each peer's XRDY barrier as soon as its
     // last PV product was done)
     bool ok = warp_wait_cluster(bar0 + 8 * B_XRDY, 0, abort_flag, p.timeout_ns, lane);
@@ -752,10 +756,11 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
     for (int gi = 1; gi < P; ++gi) {
         const uint32_t g = (me + (uint32_t)gi) % (uint32_t)P;   // peers in a rotated order
         const uint32_t dst = mapa_shared(sbase + OFF_KV + me * SLOT_BYTES, g);
+        const uint32_t rbar = mapa_shared(bar0 + 8 * B_XFULL, g);
         if (t < HP) {
             const uint32_t xs = mapa_shared(sbase + OFF_XSTAT + (me * 2 * HP + t) * 4, g);
-            st_cluster_f32(xs, m_s[g * HP + t]);
-            st_cluster_f32(xs + 4 * HP, lt[g * HP + t]);
+            st_async_b32(xs, __float_as_uint(m_s[g * HP + t]), rbar);
+            st_async_b32(xs + 4 * HP, __float_as_uint(lt[g * HP + t]), rbar);
         }
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -773,15 +778,10 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
             }
 #pragma unroll
             for (int i = 0; i < HP; i += 2)
-                st_cluster_b32(dst + (uint32_t)(((i / 2) * D + 128 * d + fl) * 4),
-                               pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
+                st_async_b32(dst + (uint32_t)(((i / 2) * D + 128 * d + fl) * 4),
+                             pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), rbar);
         }
     }
-    // every thread's stores are ordered before the arrivals below
-    fence_acq_rel_cluster();
-    bar_sync(1, SMX_THREADS);
-    if (t < P && t != (int)me)
-        mbar_arrive_remote(mapa_shared(bar0 + 8 * B_XFULL, (uint32_t)t));
 
     ok = warp_wait_cluster(bar0 + 8 * B_XFULL, 0, abort_flag, p.timeout_ns, lane);
     if (bar_red_or(1, SMX_THREADS, !ok || *abort_flag))
@@ -1138,7 +1138,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(const __grid_constant_
         }
         mbar_init(bar0 + 8 * B_DONE, 1);
         mbar_init(bar0 + 8 * B_XRDY, p.split ? (uint32_t)(p.pieces - 1) : 1u);
-        mbar_init(bar0 + 8 * B_XFULL, p.split ? (uint32_t)(p.pieces - 1) : 1u);
+        mbar_init(bar0 + 8 * B_XFULL, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&p.tm_q);

@@ -128,21 +128,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+// Asynchronous store into another CTA's shared memory of the cluster; its 4
+// bytes complete a transaction on that CTA's mbarrier `cluster_bar`.
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t cluster_bar)
 {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Orders this thread's earlier memory accesses (including stores into other
-// CTAs' shared memory) before its later ones, at cluster scope.
-__device__ __forceinline__ void fence_acq_rel_cluster()
-{
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+                 "r"(cluster_bar)
+                 : "memory");
 }
 
 // Arrive on an mbarrier of another CTA of the cluster; releases this thread's
