@@ -59,14 +59,14 @@ TRAFFIC_SOURCES = {
     "decode_fp4": ("attn",), "fused_tail_fp8": ("attn", "gemm"),
 }
 MEASURED_TRAFFIC = {
-    "decode": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 46_876_188),
-    "long_decode": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 87_940_807),
-    "prefill": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 1_055_243_040),
-    "fused_tail": ("fccab286eb25f06cf57fc0003945371c2ee4d7ad20dbfdb1f9d11bfe4df3cfcf", 1_794_871_232),
-    "block_tail": ("fccab286eb25f06cf57fc0003945371c2ee4d7ad20dbfdb1f9d11bfe4df3cfcf", 2_784_149_248),
+    "decode": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 46_603_662),
+    "long_decode": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 87_609_145),
+    "prefill": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 1_054_993_248),
+    "fused_tail": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 1_793_199_296),
+    "block_tail": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 2_777_436_704),
     "topk": ("8bee89868215d32e69245f02aef9a050199e46091e6e3bd6673116ad24b2aa48", 139_249_010),
-    "decode_fp4": ("152765113079553e884f19e2ba61f56dd01cd14ec5fdf65d693090fe3a8eaf2f", 25_182_643),
-    "fused_tail_fp8": ("fccab286eb25f06cf57fc0003945371c2ee4d7ad20dbfdb1f9d11bfe4df3cfcf", 1_835_902_592),
+    "decode_fp4": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 25_186_458),
+    "fused_tail_fp8": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 1_834_442_688),
 }
 
 
