@@ -64,7 +64,7 @@ MEASURED_TRAFFIC = {
     "prefill": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 1_054_993_248),
     "fused_tail": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 1_793_199_296),
     "block_tail": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 2_777_436_704),
-    "topk": ("8bee89868215d32e69245f02aef9a050199e46091e6e3bd6673116ad24b2aa48", 139_249_010),
+    "topk": ("cb7ef0343156eb0625f1156c9ccc55d87b93ab8c532c82af6d0f18a3fe19ce5f", 139_372_857),
     "decode_fp4": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 25_186_458),
     "fused_tail_fp8": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 1_834_442_688),
 }

@@ -12,9 +12,9 @@
 // One CTA per row.  Scores become order-preserving 32-bit keys; a three-pass
 // radix select (11, 11 and 10 bits, most significant first) finds the k-th
 // largest key: each pass histograms the keys that share the prefix chosen so
-// far into 2048 bins, and a block-wide scan over the bins, largest first
-// (eight per thread), picks the bin that holds the k-th key; the search ends
-// early once that bin is taken whole.  The first pass is folded into the
+// far into 2048 bins, and one warp scans the bins, largest first (64 a lane,
+// then two a lane within the lane's range that holds the k-th key), to pick
+// the bin that holds it; the search ends early once that bin is taken whole.  The first pass is folded into the
 // pass that computes the keys, which also finds the last selectable
 // position: the later passes stop there.  The ordered pass gives each warp a
 // contiguous range of positions.  When every key above the threshold is taken
@@ -53,39 +53,62 @@ __device__ __forceinline__ uint32_t key_of(float x)
     return x > -INFINITY ? kk : 0u;
 }
 
-// Inclusive block-wide sum of one int per thread; also returns the total.
-__device__ __forceinline__ int block_scan(int v, int *warp_sums, int &total)
+static_assert(BINS == 32 * 64, "64 histogram bins per lane in the bin search");
+
+// One warp: the bin of the need-th largest key, counting from the top bin
+// down.  Lane l sums bins 2047 - 64l down to 1984 - 64l (its 16-byte loads
+// rotated by l, so that eight lanes read eight different bank groups), a scan
+// over the lanes finds the lane whose range holds the key, and the warp then
+// scans that range two bins a lane.  Gives the bin, the keys still needed
+// within it and whether they are all of its keys; returns false instead, with
+// nothing found, when `all_if_few` is set and the histogram's total is at
+// most `need` (every key is taken).
+__device__ __forceinline__ bool find_bin(const int *hist, int need, bool all_if_few, int lane, int &bin,
+                                         int &remaining, bool &whole)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
+    const int base = BINS - 64 * (lane + 1);
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int4 v = *reinterpret_cast<const int4 *>(&hist[base + 4 * ((i + lane) & 15)]);
+        sum += v.x + v.y + v.z + v.w;
+    }
+    int cum = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        const int y = __shfl_up_sync(0xffffffffu, cum, o);
         if (lane >= o)
-            x += y;
+            cum += y;
     }
-    if (lane == 31)
-        warp_sums[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int s = lane < WARPS ? warp_sums[lane] : 0;
+    if (all_if_few && __shfl_sync(0xffffffffu, cum, 31) <= need)
+        return false;
+    const unsigned hit = __ballot_sync(0xffffffffu, cum >= need);
+    const int L = hit != 0u ? __ffs(hit) - 1 : 31;
+    const int before = __shfl_sync(0xffffffffu, cum - sum, L);
+    const int need2 = need - before;
+    // lane i: bins 63 - 2i (hi) and 62 - 2i (lo) of lane L's range
+    const int b2 = BINS - 64 * (L + 1) + 62 - 2 * lane;
+    const int2 pr = *reinterpret_cast<const int2 *>(&hist[b2]);
+    const int pair = pr.x + pr.y;
+    int cp = pair;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o)
-                s += y;
-        }
-        if (lane < WARPS)
-            warp_sums[lane] = s;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, cp, o);
+        if (lane >= o)
+            cp += y;
     }
-    __syncthreads();
-    total = warp_sums[WARPS - 1];
-    const int before = warp > 0 ? warp_sums[warp - 1] : 0;
-    __syncthreads();
-    return before + x;
+    const unsigned hit2 = __ballot_sync(0xffffffffu, cp >= need2);
+    const int I = hit2 != 0u ? __ffs(hit2) - 1 : 31;
+    const int run = cp - pair;   // keys in the bins above this lane's pair
+    const bool in_hi = run + pr.y >= need2;
+    const int my_bin = in_hi ? b2 + 1 : b2;
+    const int my_rem = in_hi ? need2 - run : need2 - run - pr.y;
+    const bool my_whole = in_hi ? run + pr.y == need2 : run + pr.y + pr.x == need2;
+    bin = __shfl_sync(0xffffffffu, my_bin, I);
+    remaining = __shfl_sync(0xffffffffu, my_rem, I);
+    whole = __shfl_sync(0xffffffffu, (int)my_whole, I) != 0;
+    return true;
 }
-
-static_assert(THREADS * 8 == BINS, "eight histogram bins per thread");
 // positions a warp can stage in its segment of the histogram's memory (16 bits each)
 constexpr int STAGE_PER_WARP = BINS * 2 / WARPS;   // 512
 
@@ -96,11 +119,11 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
 {
     extern __shared__ __align__(16) uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
     __shared__ __align__(16) int hist[BINS];
-    __shared__ int warp_sums[WARPS];
     __shared__ int wcount[2][WARPS];
     __shared__ uint32_t sel_prefix;
     __shared__ int sel_remaining;
     __shared__ bool sel_whole;
+    __shared__ bool sel_all;
     __shared__ int last_valid;
     const int64_t row = blockIdx.x;
     const float *src = scores + row * row_stride;
@@ -137,8 +160,8 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
     // bits and the last selectable position: the later passes stop after it
     // (a causal row ends in masked positions).  A thread visits its
     // positions in increasing order, so the last one it saw is its largest.
-    for (int i = t; i < BINS; i += THREADS)
-        hist[i] = 0;
+    for (int i = t; i < BINS / 4; i += THREADS)
+        reinterpret_cast<int4 *>(hist)[i] = make_int4(0, 0, 0, 0);
     if (t == 0)
         last_valid = -1;
     __syncthreads();
@@ -176,10 +199,11 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    if (kk[i] != 0u) {   // 0 past the end
+                    if (kk[i] != 0u)   // 0 past the end
                         atomicAdd(&hist[kk[i] >> 21], 1);
-                        last = j + i;
-                    }
+                // the last selectable position, to the end of its group of four
+                if ((kk[0] | kk[1] | kk[2] | kk[3]) != 0u)
+                    last = j + 3;
             }
         }
     } else {
@@ -207,7 +231,7 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
     if (lane == 0)
         atomicMax(&last_valid, last);
     __syncthreads();
-    const int Lv = last_valid + 1;   // positions from Lv on are all masked
+    const int Lv = min(last_valid + 1, L);   // positions from Lv on are all masked
 
     // threshold: every key above thr is taken, and the first take_eq keys
     // equal to it.  With no more than k selectable keys (the histogram's
@@ -224,8 +248,8 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
             const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
             const uint32_t dmask = pass < 2 ? 2047u : 1023u;
             if (pass > 0) {
-                for (int i = t; i < BINS; i += THREADS)
-                    hist[i] = 0;
+                for (int i = t; i < BINS / 4; i += THREADS)
+                    reinterpret_cast<int4 *>(hist)[i] = make_int4(0, 0, 0, 0);
                 __syncthreads();
                 for (int base = 0; base < Lv; base += 4 * THREADS * SWEEP_VEC) {
                     uint32_t kb[4 * SWEEP_VEC];
@@ -242,41 +266,29 @@ __global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const flo
                 }
                 __syncthreads();
             }
-            // thread i holds bins 2047 - 8i down to 2040 - 8i: the running
-            // count from the top first reaches `need` in the bin of the
-            // need-th largest key
-            const int b0 = BINS - 8 - 8 * t;
-            const int4 lo = *reinterpret_cast<const int4 *>(&hist[b0]);
-            const int4 hi = *reinterpret_cast<const int4 *>(&hist[b0 + 4]);
-            const int c[8] = {hi.w, hi.z, hi.y, hi.x, lo.w, lo.z, lo.y, lo.x};
-            int own = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                own += c[i];
-            int tot = 0;
-            const int cum = block_scan(own, warp_sums, tot);
-            if (pass == 0 && tot <= k)   // the block's total: the same in every thread
-                break;
-            if (cum >= need && cum - own < need) {
-                int run = cum - own;
-                bool found = false;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (!found && run + c[i] >= need) {
-                        sel_prefix = prefix | ((uint32_t)(b0 + 7 - i) << shift);
-                        sel_remaining = need - run;
-                        sel_whole = run + c[i] == need;
-                        found = true;
-                    }
-                    run += c[i];
+            // one warp finds the bin of the need-th largest key; with no more
+            // than k selectable keys in the first pass (the histogram's total),
+            // all of them are taken
+            if (warp == 0) {
+                int bin = 0, rem = 0;
+                bool wh = false;
+                const bool found = find_bin(hist, need, pass == 0, lane, bin, rem, wh);
+                if (lane == 0) {
+                    sel_all = !found;
+                    sel_prefix = prefix | ((uint32_t)bin << shift);
+                    sel_remaining = rem;
+                    sel_whole = wh;
                 }
             }
             __syncthreads();
+            if (sel_all)   // the same in every thread
+                break;
             prefix = sel_prefix;
             need = sel_remaining;
             mask |= dmask << shift;
             const bool whole = sel_whole;
-            __syncthreads();
+            // (warp 0 writes the selection again only after the next pass's
+            // two barriers, which every thread reaches after reading it)
             if (whole) {   // every key of the bin is taken
                 thr = prefix - 1u;
                 take_eq = 0;
