@@ -33,6 +33,10 @@
  *     Two calls that share a workspace must not run concurrently.
  *   - Fast path only: H == 64 heads, D == 512 features; other shapes return
  *     SA_ERR_UNSUPPORTED.  1 <= K <= SA_MAX_K, or K == 0 (all-zero output).
+ *   - The library is also built with address checks in its kernels
+ *     (libsa_checked.so, this same ABI): every address a kernel computes from
+ *     run-time values is tested before use, and a failed test skips the
+ *     access and sets the error word's bounds bit (SA_ERR_BOUNDS).
  */
 #ifndef SA_H_
 #define SA_H_
@@ -51,7 +55,9 @@ typedef enum {
     SA_ERR_WORKSPACE = 3,     /* workspace smaller than the *_workspace_size query */
     SA_ERR_INDEX = 4,         /* device saw an index outside [-1, N); it was skipped */
     SA_ERR_TIMEOUT = 5,       /* a bounded device wait ran out; outputs are invalid */
-    SA_ERR_CUDA = 6           /* a CUDA runtime/driver call failed (no device, launch error) */
+    SA_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed (no device, launch error) */
+    SA_ERR_BOUNDS = 7         /* checked build only: an address check failed and the access was
+                                 skipped; outputs are invalid */
 } sa_status;
 
 typedef enum { SA_BF16 = 0, SA_F32 = 1 } sa_dtype;
@@ -294,7 +300,8 @@ sa_status sa_sparse_attn_noalloc(const void *q, const void *kv, const float *sin
 
 /*
  * Synchronise `stream`, read the workspace error word, clear it, and return
- * SA_ERR_TIMEOUT, SA_ERR_INDEX (in that order of precedence) or SA_OK.
+ * SA_ERR_BOUNDS, SA_ERR_TIMEOUT, SA_ERR_INDEX (in that order of precedence)
+ * or SA_OK.
  */
 sa_status sa_check_errors(void *workspace, void *stream);
 

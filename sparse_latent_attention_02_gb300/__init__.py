@@ -16,7 +16,7 @@ import threading
 
 import torch
 
-from ._build import LIB as _LIB_PATH, build  # noqa: F401
+from ._build import LIB as _LIB_PATH, LIB_CHECKED as _LIB_CHECKED_PATH, build  # noqa: F401
 
 __all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_two_source_fp4", "sparse_attn_rope_wo_a",
            "sparse_attn_block_tail",
@@ -25,7 +25,7 @@ __all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_two_source_fp4"
 
 HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
 _STATUS = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_WORKSPACE",
-           4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA"}
+           4: "SA_ERR_INDEX", 5: "SA_ERR_TIMEOUT", 6: "SA_ERR_CUDA", 7: "SA_ERR_BOUNDS"}
 EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_two_source",
            "sa_sparse_attn_rope_wo_a_workspace_size", "sa_sparse_attn_rope_wo_a",
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
@@ -45,12 +45,15 @@ _lock = threading.Lock()
 _lib = None
 
 
-def library(path: str | None = None) -> ctypes.CDLL:
-    """Load ``libsa.so`` (raises if it has not been built)."""
+def library(path: str | None = None, checked: bool = False) -> ctypes.CDLL:
+    """Load ``libsa.so`` (raises if it has not been built) and make it the
+    library every call of this module uses.  ``checked`` loads the build whose
+    kernels test their computed addresses (``libsa_checked.so``, same ABI; a
+    failed test surfaces as SA_ERR_BOUNDS)."""
     global _lib
     with _lock:
-        if _lib is None or path is not None:
-            p = path or _LIB_PATH
+        if _lib is None or path is not None or checked:
+            p = path or (_LIB_CHECKED_PATH if checked else _LIB_PATH)
             if not os.path.exists(p):
                 raise RuntimeError(f"{p} is missing: build the CUDA library first "
                                    "(sparse_latent_attention_02_gb300.build())")

@@ -2,7 +2,10 @@
 
 nvcc for sm_103a only, one translation unit per process, linked with the
 static CUDA runtime so that the library loads on machines without a GPU
-(every call then returns SA_ERR_CUDA).
+(every call then returns SA_ERR_CUDA).  The same sources are also built with
+SA_CHECKED into ``libsa_checked.so``: the same ABI, with the kernels testing
+the addresses they compute from run-time values (a failed test sets the
+error word's bounds bit, SA_ERR_BOUNDS, and skips the access).
 """
 from __future__ import annotations
 
@@ -16,7 +19,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libsa.so")
+LIB_CHECKED = os.path.join(PKG, "libsa_checked.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
+# library -> (extra nvcc flags, object directory)
+VARIANTS = {LIB: ([], BUILD_DIR), LIB_CHECKED: (["-DSA_CHECKED"], os.path.join(BUILD_DIR, "checked"))}
 SOURCES = ["sa_attn.cu", "sa_gemm.cu", "sa_topk.cu", "sa_api.cu", "sa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
@@ -36,37 +42,46 @@ def _inputs():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+    """Build both libraries (the translation units of both in one pool) and
+    return the path of ``libsa.so``."""
+    todo = [lib for lib in VARIANTS if force or not up_to_date(lib)]
+    if not todo:
         return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
+    for lib in todo:
+        os.makedirs(VARIANTS[lib][1], exist_ok=True)
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        lib, src = job
+        defs, objdir = VARIANTS[lib]
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *ARCH, *FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src} ({os.path.basename(lib)}):\n{r.stdout}\n{r.stderr}")
         if verbose and (r.stdout or r.stderr):
             print(r.stdout + r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(lib, src) for lib in todo for src in SOURCES]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    for lib in todo:
+        mine = [o for (l, _), o in zip(jobs, objs) if l == lib]
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *mine]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed ({os.path.basename(lib)}):\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB
 
 

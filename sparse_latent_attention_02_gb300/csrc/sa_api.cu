@@ -633,6 +633,8 @@ sa_status sa_check_errors(void *workspace, void *stream)
         if (cudaMemcpy(workspace, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess)
             return SA_ERR_CUDA;
     }
+    if (w & ERRBIT_BOUNDS)
+        return SA_ERR_BOUNDS;
     if (w & ERRBIT_TIMEOUT)
         return SA_ERR_TIMEOUT;
     if (w & ERRBIT_INDEX)
@@ -650,6 +652,7 @@ const char *sa_status_string(sa_status s)
     case SA_ERR_INDEX: return "an index outside [-1, N) was seen and skipped";
     case SA_ERR_TIMEOUT: return "a bounded device wait ran out";
     case SA_ERR_CUDA: return "CUDA runtime or driver error";
+    case SA_ERR_BOUNDS: return "an address check of the checked build failed; the access was skipped";
     }
     return "unknown status";
 }

@@ -185,8 +185,9 @@ __device__ __forceinline__ const uint16_t *kv_row(const AttnParams &p, int64_t b
 __device__ __forceinline__ void stage_list(const AttnParams &p, const Seg &s, uint32_t raw, int lane)
 {
     const int32_t *il = p.idx + s.q * (int64_t)p.K;
-    for (int j = s.j0 + lane; j < s.j1; j += 32)
-        cp_async4(raw + 4u * (uint32_t)(j - s.j0), il + j);
+    if (in_bounds(s.q < p.BT && s.j0 >= 0 && s.j1 <= p.K && s.j1 - s.j0 <= SA_MAX_K, p.err))
+        for (int j = s.j0 + lane; j < s.j1; j += 32)
+            cp_async4(raw + 4u * (uint32_t)(j - s.j0), il + j);
     cp_async_commit();
 }
 
@@ -215,6 +216,25 @@ __device__ __forceinline__ int compact_staged(const int32_t *raw, int len, int N
         }
     }
     return n;
+}
+
+// Checked build: [ptr, ptr + bytes) lies inside the rows of the source that
+// list index v reads (every batch element's rows of that source).
+template <bool TWO>
+__device__ __forceinline__ bool row_inside(const AttnParams &p, int v, const void *ptr, size_t bytes)
+{
+    const int64_t B = p.BT / p.T;
+    if (TWO && v >= p.W)
+        return inside(ptr, bytes, p.kv2, ((size_t)(B - 1) * (size_t)p.kv2_bstride + (size_t)(p.N - p.W)) * D * 2);
+    return inside(ptr, bytes, p.kv, ((size_t)(B - 1) * (size_t)p.kv_bstride + (size_t)(TWO ? p.W : p.N)) * D * 2);
+}
+
+// Checked build: the same for the fp4 codes (D/2 bytes a row) and scales (D/16).
+__device__ __forceinline__ bool fp4_inside(const AttnParams &p, const uint8_t *ptr, size_t bytes, bool scales)
+{
+    const int64_t B = p.BT / p.T;
+    const size_t rows = (size_t)(B - 1) * (size_t)p.kv2_bstride + (size_t)(p.N - p.W);
+    return scales ? inside(ptr, bytes, p.kv2_scales, rows * (D / 16)) : inside(ptr, bytes, p.kv2_codes, rows * (D / 2));
 }
 
 // Warm L2 with latent rows (whole warp, one line prefetch per 128 bytes):
@@ -296,9 +316,13 @@ __device__ __forceinline__ bool load_q(const AttnParams &p, uint32_t sbase, cons
         return false;
     if (lane == 0) {
         const uint32_t bq = bar0 + 8 * B_QFULL;
-        mbar_arrive_expect_tx(bq, Q_BYTES);
-        for (int kb = 0; kb < 8; ++kb)
-            tma_load_2d(sbase + OFF_Q + kb * QBLK_BYTES, &p.tm_q, kb * 64, (int32_t)(s.q * H), bq);
+        if (in_bounds(s.q < p.BT, p.err)) {
+            mbar_arrive_expect_tx(bq, Q_BYTES);
+            for (int kb = 0; kb < 8; ++kb)
+                tma_load_2d(sbase + OFF_Q + kb * QBLK_BYTES, &p.tm_q, kb * 64, (int32_t)(s.q * H), bq);
+        } else {
+            mbar_arrive(bq);
+        }
     }
     ++q_loads;
     return true;
@@ -483,10 +507,12 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                         if (rv[j] >= p.W) {
                             const size_t cr = (size_t)bidx * (size_t)p.kv2_bstride + (size_t)(rv[j] - p.W);
                             const int d = grp + 2 * e;
-                            code[e][j] = __ldg(reinterpret_cast<const uint4 *>(p.kv2_codes + cr * (D / 2) + 64 * d +
-                                                                               16 * qq));
+                            const uint8_t *cp = p.kv2_codes + cr * (D / 2) + 64 * d + 16 * qq;
                             const uint8_t *sp = p.kv2_scales + cr * (D / 16) + 8 * d + 2 * qq;
-                            scl[e][j] = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+                            if (in_bounds(fp4_inside(p, cp, 16, false) && fp4_inside(p, sp, 2, true), p.err)) {
+                                code[e][j] = __ldg(reinterpret_cast<const uint4 *>(cp));
+                                scl[e][j] = (uint32_t)__ldg(sp) | ((uint32_t)__ldg(sp + 1) << 8);
+                            }
                         }
                     }
                 }
@@ -505,7 +531,11 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                         const int r = r0 + 2 * i;
                         const uint32_t dst = sbase + OFF_KV + sl * SLICE_BYTES + r * 128 + ((ch ^ (r & 7)) << 4);
                         const uint16_t *src = row_ptr(row[i] < 0 ? 0 : row[i]) + sl * 64 + ch * 8;
-                        cp_async16(dst, src, row[i] < 0 ? 0u : 16u);
+                        // (a row that fails its source check is zero-filled from a
+                        // valid address, like an empty slot)
+                        const bool live = row[i] >= 0 && in_bounds(row_inside<TWO>(p, row[i], src, 16), p.err);
+                        if (in_bounds(r < CH && sl < 8, p.err))
+                            cp_async16(dst, live || row[i] < 0 ? src : row_ptr(0), live ? 16u : 0u);
                     }
                 } else {
                     // quarter qq: slice 2d + qq / 2, 16-byte chunks 4 (qq % 2) .. +3
@@ -514,6 +544,8 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                     for (int j = 0; j < 2; ++j) {
                         const int r = rf + 8 * j, v = rv[j];
                         const uint32_t roff = OFF_KV + sl * SLICE_BYTES + r * 128;
+                        if (!in_bounds(r < CH && sl < 8, p.err))
+                            continue;
                         if (v >= p.W) {
                             uint32_t s0, s1;
                             scales_x2112(scl[e][j], s0, s1);
@@ -528,10 +560,12 @@ __device__ void gather_role(const AttnParams &p, uint8_t *smem, uint32_t sbase, 
                             const uint16_t *src =
                                 v >= 0 ? kvb + (size_t)v * D + 128 * d + 32 * qq
                                        : (p.W > 0 ? kvb : reinterpret_cast<const uint16_t *>(p.kv2_codes));
+                            const bool live = v >= 0 && in_bounds(row_inside<true>(p, v, src, 64), p.err);
+                            const uint16_t *dead = v >= 0 ? kvb : src;   // a valid address for no bytes
 #pragma unroll
                             for (int m = 0; m < 4; ++m)
-                                cp_async16(sbase + roff + (((ch0 + m) ^ (r & 7)) << 4), v >= 0 ? src + 8 * m : src,
-                                           v < 0 ? 0u : 16u);
+                                cp_async16(sbase + roff + (((ch0 + m) ^ (r & 7)) << 4), live ? src + 8 * m : dead,
+                                           live ? 16u : 0u);
                         }
                     }
                 }
@@ -865,7 +899,8 @@ __device__ bool cluster_merge(const AttnParams &p, uint8_t *smem, uint32_t sbase
                 o[i] = odd ? (o[i] * cth - other * sth) : (o[i] * cth + other * sth);
             }
         }
-        if (p.out_f32) {
+        if (!in_bounds(s.q < p.BT && (int)(me + 1) * HP <= H && f < D, p.err)) {
+        } else if (p.out_f32) {
             float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + (size_t)(me * HP) * D + f;
 #pragma unroll
             for (int i = 0; i < HP; ++i)
@@ -1088,7 +1123,8 @@ __device__ void softmax_role(const AttnParams &p, uint8_t *smem, uint32_t sbase,
                     u[i] = __float_as_uint(odd ? (o * cth - other * sth) : (o * cth + other * sth));
                 }
             }
-            if (p.out_f32) {
+            if (!in_bounds(s.q < p.BT && hb + 32 <= H && dim < D, p.err)) {
+            } else if (p.out_f32) {
                 float *po = reinterpret_cast<float *>(p.out) + (size_t)s.q * (H * D) + (size_t)hb * D + dim;
 #pragma unroll
                 for (int i = 0; i < 32; ++i)

@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1) wo_a_fp8_kernel(const __grid_
                     uint32_t v[32];
                     tmem_ld32(ta + 32 * c, v);
                     tmem_wait_ld();
-                    if (m < p.M) {
+                    if (m < p.M && in_bounds(inside(yrow + 32 * c, 64, p.y, (size_t)p.M * p.G * p.R * 2), p.err)) {
                         uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * c);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(THREADS, 1) wo_a_pair_kernel(const __grid_cons
                 uint32_t v[32];
                 tmem_ld32(ta + 32 * c, v);
                 tmem_wait_ld();
-                if (m < p.M) {
+                if (m < p.M && in_bounds(inside(yrow + 32 * c, 64, p.y, (size_t)p.M * p.G * p.R * 2), p.err)) {
                     uint4 *dst = reinterpret_cast<uint4 *>(yrow + 32 * c);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)

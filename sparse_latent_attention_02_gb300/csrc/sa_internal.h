@@ -12,6 +12,33 @@ namespace sa {
 // Bits of the device error word (first 4 bytes of every workspace).
 constexpr uint32_t ERRBIT_INDEX = 1u;
 constexpr uint32_t ERRBIT_TIMEOUT = 2u;
+constexpr uint32_t ERRBIT_BOUNDS = 4u;   // checked build: an address check failed
+
+#ifdef __CUDACC__
+// The checked build (compiled with SA_CHECKED) tests the addresses the
+// kernels compute from run-time values before it uses them: a failed test
+// sets ERRBIT_BOUNDS in the error word and the caller skips the access.  In
+// the normal build the test compiles away.
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t *err)
+{
+#ifdef SA_CHECKED
+    if (!ok)
+        atomicOr(err, ERRBIT_BOUNDS);
+    return ok;
+#else
+    (void)ok;
+    (void)err;
+    return true;
+#endif
+}
+
+// [p, p + bytes) lies inside [base, base + extent)
+__device__ __forceinline__ bool inside(const void *p, size_t bytes, const void *base, size_t extent)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(base);
+    return a >= b && a - b <= extent && bytes <= extent - (a - b);
+}
+#endif
 
 // Workspace layout of the attention call: [0, 256) header (error word).
 constexpr size_t WS_HEADER = 256;

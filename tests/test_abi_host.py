@@ -34,6 +34,16 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(sa.EXPORTS)
 
 
+def test_checked_build_exports_the_same_symbols(lib):
+    """The build with address checks in its kernels (libsa_checked.so) is
+    built beside libsa.so and exports the same ABI."""
+    checked = ctypes.CDLL(sa._LIB_CHECKED_PATH)
+    for n in declared_functions():
+        assert hasattr(checked, n), n
+    checked.sa_status_string.restype = ctypes.c_char_p
+    assert b"checked build" in checked.sa_status_string(7)
+
+
 def _declarations():
     """name -> (return type, [parameter types]) of every function in sa.h."""
     text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
@@ -76,7 +86,7 @@ def test_binding_signatures_match_the_header(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = lib.sa_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.sa_status_string(99).decode() == "unknown status"
