@@ -59,14 +59,14 @@ TRAFFIC_SOURCES = {
     "decode_fp4": ("attn",), "fused_tail_fp8": ("attn", "gemm"),
 }
 MEASURED_TRAFFIC = {
-    "decode": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 46_603_662),
-    "long_decode": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 87_609_145),
-    "prefill": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 1_054_993_248),
-    "fused_tail": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 1_793_199_296),
-    "block_tail": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 2_777_436_704),
+    "decode": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 46_600_903),
+    "long_decode": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 87_575_723),
+    "prefill": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 1_055_305_024),
+    "fused_tail": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 1_789_614_368),
+    "block_tail": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 2_776_463_264),
     "topk": ("cb7ef0343156eb0625f1156c9ccc55d87b93ab8c532c82af6d0f18a3fe19ce5f", 139_372_857),
-    "decode_fp4": ("7ad7cc400945712bd77e03602cce76965671ce40aa1e6cae0feb08240361e383", 25_186_458),
-    "fused_tail_fp8": ("91111ff8d7a08772251d36257971f9a5e6750a281fc2866d55b16917096a34c3", 1_834_442_688),
+    "decode_fp4": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 25_186_662),
+    "fused_tail_fp8": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 1_831_613_824),
 }
 
 
