@@ -369,8 +369,8 @@ def test_block_tail_workload_sampled():
     (24, 1030, 64, "tiny"),       # subnormals, signed zeros and -inf: subnormals are not zero
     (4, 16383, 512, "full"),      # the longest row whose keys stay in shared memory
     (4, 16385, 512, "full"),      # the shortest row read again from L2 on every pass
-    (16, 1024, 512, "cluster"),   # the first pass's bin holds 1024 keys: the most its list takes
-    (16, 1025, 512, "cluster"),   # 1025 keys: every later pass sweeps the whole row
+    (16, 1024, 512, "cluster"),   # every key in one first-pass bin: the later digits decide
+    (16, 1025, 512, "cluster"),   # the same with a ragged last group of four keys
     (16, 4096, 512, "cluster"),   # scores 1.1 + 1e-4 N(0,1): the low digits decide
     (16, 4096, 512, "flat"),      # all equal but 10% masked: ties decide every position
     (8, 20000, 512, "cluster"),   # the same with the keys read again from L2
