@@ -18,6 +18,11 @@ wrappers:
 * :func:`dequant_fp8_weight` -- the fp8 ``wo_a`` weight (E4M3, fp32 scale per
   128 x 128 block) dequantized to bf16, as the page's conversion does before
   the einsum.
+* :func:`fp4_quantize`  -- ``fp4_act_quant(latent, 16, True,
+  scale_dtype=torch.float8_e4m3fn)`` of the "DeepSeek-V4.1 > 40 layers" page,
+  read as an E4M3 scale of amax / 6 per 16 features and e2m1 codes of x /
+  scale, both rounded to nearest with ties to even (:func:`e4m3_encode`,
+  :func:`e2m1_encode`), in the packed layout :func:`dequant_fp4` reads.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against a dense
 masked brute force, closed forms and invariants; nothing here is "parity
@@ -174,6 +179,62 @@ def dequant_fp4(codes, scales) -> np.ndarray:
     val = np.where(nib & 8, -mag, mag)
     sc = np.repeat(e4m3_values(scales), 16, axis=-1)
     return val * sc
+
+
+def _nearest_even(x, grid, even) -> np.ndarray:
+    """Index into `grid` (ascending, non-negative) of the value nearest to each
+    |x|, halfway cases to the index whose `even` flag is set; |x| above the
+    largest grid value takes the largest (saturation)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    g = np.asarray(grid, dtype=np.float64)
+    hi = np.clip(np.searchsorted(g, a, side="left"), 0, len(g) - 1)   # first grid value >= a
+    lo = np.clip(hi - 1, 0, len(g) - 1)
+    dlo, dhi = a - g[lo], g[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(np.asarray(even)[lo], lo, hi)))
+    return np.where(a >= g[-1], len(g) - 1, pick)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Values -> OCP FP8 E4M3 ("fn") bytes: the nearest finite E4M3 value,
+    halfway cases to the even mantissa, magnitudes past 448 to 448; the sign
+    kept (also for results of zero)."""
+    x = np.asarray(x, dtype=np.float64)
+    mags = np.arange(0x7F, dtype=np.int64)                  # 0x00 .. 0x7E: every finite magnitude
+    idx = _nearest_even(x, e4m3_values(mags), (mags & 1) == 0)
+    return (idx | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def e2m1_encode(x) -> np.ndarray:
+    """Values -> e2m1 codes (bit 3 sign, bits 2..0 index 0, .5, 1, 1.5, 2, 3,
+    4, 6): the nearest magnitude, halfway cases to the even index, past 6 to
+    6; the sign kept (also for results of zero)."""
+    x = np.asarray(x, dtype=np.float64)
+    idx = _nearest_even(x, E2M1_MAGNITUDES, np.arange(8) % 2 == 0)
+    return (idx | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+
+def fp4_quantize(latent_bf16) -> tuple[np.ndarray, np.ndarray]:
+    """The "DeepSeek-V4.1 > 40 layers" page's `fp4_act_quant(latent, 16, True,
+    scale_dtype=torch.float8_e4m3fn)` (its body is not on the pages; this is
+    the reading the library implements): per group of 16 features, the scale
+    is E4M3(amax / 6) (amax the group's largest magnitude, 6 the largest e2m1
+    value, the division in fp32), each value's code is e2m1(x / scale) (fp32
+    division; a zero scale gives codes of zero with x's sign).
+
+    latent_bf16: bf16 bit patterns uint16 [..., D], D % 16 == 0, finite or
+    infinite values.  Returns (codes uint8 [..., D/2], low nibble = even
+    feature; scales uint8 [..., D/16]) in the layout of `dequant_fp4`."""
+    u = np.asarray(latent_bf16, dtype=np.uint16)
+    x = (u.astype(np.uint32) << 16).view(np.float32)
+    g = x.reshape(*x.shape[:-1], x.shape[-1] // 16, 16)
+    amax = np.max(np.abs(g), axis=-1)
+    sb = e4m3_encode(amax / np.float32(6.0))                  # fp32 division
+    s = e4m3_values(sb).astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(s > 0, g / np.where(s > 0, s, np.float32(1)), g * np.float32(0))   # fp32 division
+    c = e2m1_encode(v).reshape(*x.shape[:-1], x.shape[-1])
+    codes = (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    return codes, sb
 
 
 def bf16_bits_exact(x) -> np.ndarray:

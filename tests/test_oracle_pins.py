@@ -530,3 +530,74 @@ def test_fp8_weight_matches_torch_dequantization_and_block_layout():
         assert np.array_equal(got[i], lib), i
     with pytest.raises(ValueError):
         oracle.dequant_fp8_weight(w8, sc[:2])
+
+
+# ---------------------------------------------------------------- fp4 quantizer
+
+def test_e4m3_encode_matches_torch_float8_rounding():
+    """The oracle's E4M3 encoding (nearest, ties to the even mantissa) against
+    PyTorch's float8_e4m3fn conversion on in-range values, with every halfway
+    point between neighbouring E4M3 values included."""
+    rng = np.random.default_rng(21)
+    x = (rng.uniform(-1, 1, 50000) * np.exp2(rng.integers(-12, 9, 50000))).astype(np.float32)
+    mags = oracle.e4m3_values(np.arange(0x7F))
+    mid = ((mags[:-1] + mags[1:]) / 2).astype(np.float32)            # exact in fp32
+    x = np.concatenate([x, mid, -mid, mags.astype(np.float32)])
+    x = x[np.abs(x) <= 448]
+    ours = oracle.e4m3_encode(x)
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, lib)
+
+
+def test_e4m3_encode_saturates_and_keeps_the_sign():
+    assert list(oracle.e4m3_encode(np.array([448.0, 464.0, 1e30, np.inf, -1e30]))) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+    assert list(oracle.e4m3_encode(np.array([0.0, -0.0, 2.0 ** -11, -(2.0 ** -11)]))) == [0x00, 0x80, 0x00, 0x80]
+
+
+def test_e2m1_encode_halfway_cases_by_hand():
+    # halfway between two magnitudes -> the even index (0, 1.0, 2.0, 4.0)
+    x = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.26, 2.6, 5.1, 7.0, np.inf, -0.0, -0.1, -3.0]
+    want = [0, 2, 2, 4, 4, 6, 6, 1, 5, 7, 7, 7, 8, 8, 8 | 5]
+    assert list(oracle.e2m1_encode(np.array(x))) == want
+
+
+def test_fp4_quantize_worked_group():
+    """One group worked by hand: amax 12 -> scale E4M3(2.0) = 0x40, then each
+    value / 2 to the nearest e2m1 magnitude."""
+    x = np.zeros(16, dtype=np.float32)
+    x[:8] = [3.0, -1.5, 0.4, 12.0, -12.0, 5.0, 2.5, -0.0]
+    codes, scales = oracle.fp4_quantize(oracle.round_bf16(x)[None])
+    assert scales[0, 0] == 0x40
+    # x / 2 = 1.5, -0.75, 0.2, 6, -6, 2.5, 1.25, -0: idx 3, 2 (tie), 0, 7, 7, 4 (tie), 2 (tie), 0
+    nib = [3, 8 | 2, 0, 7, 8 | 7, 4, 2, 8] + [0] * 8
+    want = [nib[2 * i] | (nib[2 * i + 1] << 4) for i in range(8)]
+    assert list(codes[0]) == want
+
+
+def test_fp4_quantize_round_trips_the_fp4_grid():
+    """Values on the fp4 grid whose group holds a +-6 code: decoding, then
+    quantizing again, gives the same codes and scales (amax / 6 is then the
+    scale exactly)."""
+    rng = np.random.default_rng(22)
+    rows, D = 64, 512
+    nib = rng.integers(0, 16, (rows, D))
+    g = nib.reshape(rows, D // 16, 16)
+    pos = rng.integers(0, 16, (rows, D // 16))
+    np.put_along_axis(g, pos[..., None], 7 | (8 * rng.integers(0, 2, (rows, D // 16, 1))), axis=-1)
+    codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    scales = rng.integers(0x08, 0x70, (rows, D // 16)).astype(np.uint8)    # normal scales, 6 x scale finite
+    vals = oracle.dequant_fp4(codes, scales)
+    c2, s2 = oracle.fp4_quantize(oracle.bf16_bits_exact(vals))
+    assert np.array_equal(s2, scales)
+    assert np.array_equal(c2, codes)
+
+
+def test_fp4_quantize_zero_group_and_rounded_down_scale():
+    x = np.zeros((2, 16), dtype=np.float32)
+    x[0, 3] = -0.0
+    x[1, 0] = 6.25          # amax / 6 = 1.0417 -> scale 1.0 (0x38): 6.25 saturates to code 6
+    x[1, 1] = -6.25
+    codes, scales = oracle.fp4_quantize(oracle.round_bf16(x))
+    assert scales[0, 0] == 0x00 and scales[1, 0] == 0x38
+    assert codes[0, 1] == 0x80 and np.all(np.delete(codes[0], 1) == 0)     # the -0 keeps its sign
+    assert codes[1, 0] == (7 | ((8 | 7) << 4))
