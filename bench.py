@@ -8,8 +8,9 @@ to four significant digits, the per-workload entries last).  Besides the
 contract's keys it carries, under "workloads", the other lines: long-context
 decode, prefill, the fused tail (attention, inverse RoPE, grouped wo_a), the
 block tail (plus wo_b), the top-k selection (8192 rows x 4096 scores -> 512),
-decode with fp4 compressed rows and the fused tail with an fp8 wo_a.  Each
-entry: "ms" per call, "qps" (queries/s; "rows_per_s" for top-k), the roofline
+decode with fp4 compressed rows, the fused tail with an fp8 wo_a and the fp4
+quantization of the decode workload's compressed cache.  Each entry: "ms" per
+call, "qps" (queries/s; "rows_per_s" for top-k and the quantization), the roofline
 ("bound" hbm or tensor; "ach" achieved, GB/s or TFLOP/s; "peak"; "frac";
 "traffic", measured DRAM bytes per launch of the dominant kernel, or null;
 "peak_kind" burst or sustained for tensor-bound lines) and "cpu", the fp64
@@ -53,10 +54,11 @@ CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "sparse_latent_a
 KERNEL_SRC = os.path.join(CSRC, "sa_attn.cu")
 GEMM_SRC = os.path.join(CSRC, "sa_gemm.cu")
 TOPK_SRC = os.path.join(CSRC, "sa_topk.cu")
+QUANT_SRC = os.path.join(CSRC, "sa_quant.cu")
 TRAFFIC_SOURCES = {
     "decode": ("attn",), "long_decode": ("attn",), "prefill": ("attn",),
     "fused_tail": ("attn", "gemm"), "block_tail": ("attn", "gemm"), "topk": ("topk",),
-    "decode_fp4": ("attn",), "fused_tail_fp8": ("attn", "gemm"),
+    "decode_fp4": ("attn",), "fused_tail_fp8": ("attn", "gemm"), "fp4_quant": ("quant",),
 }
 MEASURED_TRAFFIC = {
     "decode": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 46_600_903),
@@ -67,6 +69,7 @@ MEASURED_TRAFFIC = {
     "topk": ("cb7ef0343156eb0625f1156c9ccc55d87b93ab8c532c82af6d0f18a3fe19ce5f", 139_372_857),
     "decode_fp4": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 25_186_662),
     "fused_tail_fp8": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 1_831_613_824),
+    "fp4_quant": ("72256a54edd611e08447f2001cfaf57b4d99696cbe021a19194a03831af11d6b", 323_330_304),
 }
 
 
@@ -75,7 +78,7 @@ def measured_traffic(workload):
     entry = MEASURED_TRAFFIC.get(workload)
     if entry is None:
         return None
-    paths = {"attn": KERNEL_SRC, "gemm": GEMM_SRC, "topk": TOPK_SRC}
+    paths = {"attn": KERNEL_SRC, "gemm": GEMM_SRC, "topk": TOPK_SRC, "quant": QUANT_SRC}
     digest = hashlib.sha256()
     for key in TRAFFIC_SOURCES[workload]:
         with open(paths[key], "rb") as f:
@@ -578,10 +581,50 @@ def bench_fused_tail_fp8(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 
 
 
 # the additional lines that are not attention workloads, by name
+def bench_fp4_quant(steps: int, warmup: int, dev, pk: dict, cpu_s: float = 0.0) -> dict:
+    """fp4 quantization of the decode workload's compressed cache (64 batch
+    rows x 4096 latent rows x 512 features, RMS-normalised N(0,1)) into codes
+    and E4M3 group scales: one call per step, two input sets rotating (each
+    larger than L2)."""
+    import sparse_latent_attention_02_gb300 as sa
+    wl = I.WORKLOADS["decode"]
+    rows, D = wl.B * wl.C, wl.D
+    sets = []
+    for i in range(2):
+        g = torch.Generator(device=dev).manual_seed(400 + i)
+        lat = torch.empty((rows, D), dtype=torch.bfloat16, device=dev)
+        for r0 in range(0, rows, 65536):
+            r1 = min(rows, r0 + 65536)
+            lat[r0:r1] = I.rms_rows(torch.randn((r1 - r0, D), generator=g, device=dev)).to(torch.bfloat16)
+        sets.append((lat, torch.empty((rows, D // 2), dtype=torch.uint8, device=dev),
+                     torch.empty((rows, D // 16), dtype=torch.uint8, device=dev)))
+    fns = [lambda lat=lat, c=c, s=s: sa.fp4_quantize(lat, c, s) for lat, c, s in sets]
+    secs, _ = time_graph_steps(fns, steps, warmup)
+    step_s = secs / steps
+    nbytes = rows * (2 * D + D // 2 + D // 16)
+    gbs = nbytes / step_s / 1e9
+    res = {"ms_per_step": step_s * 1e3, "rows_per_s": rows / step_s, "bytes_per_step": nbytes,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "traffic": measured_traffic("fp4_quant")}}
+    if cpu_s > 0:
+        import oracle
+        n = 16384
+        bits = sets[0][0][:n].cpu().view(torch.int16).numpy().view(np.uint16)
+        t0 = time.time()
+        oracle.fp4_quantize(bits)
+        dt = time.time() - t0
+        res["cpu"] = {"value": n / dt, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                      "sample": f"{n} rows, {dt:.1f} s"}
+    del sets, fns
+    torch.cuda.empty_cache()
+    return res
+
+
 EXTRA_LINES = {
     "topk": bench_topk,
     "decode_fp4": bench_decode_fp4,
     "fused_tail_fp8": bench_fused_tail_fp8,
+    "fp4_quant": bench_fp4_quant,
 }
 
 
@@ -710,6 +753,8 @@ def run_ours(args):
                                                       per_line_cpu))
         extra["fused_tail_fp8"] = _entry(bench_fused_tail_fp8(max(3, min(args.steps, 20)), max(args.warmup, 3), dev,
                                                               pk, per_line_cpu))
+        extra["fp4_quant"] = _entry(bench_fp4_quant(max(3, min(args.steps, 50)), max(args.warmup, 3), dev, pk,
+                                                    per_line_cpu))
     sampler.stop()
     e2e = head.pop("e2e", None)
     if e2e:

@@ -258,6 +258,35 @@ sa_status sa_topk_indices(const float *scores, int64_t row_stride, int64_t rows,
                           int k, int offset, int32_t *out, void *stream);
 
 /*
+ * fp4 quantization of latent rows into the compressed-cache layout that
+ * sa_sparse_attn_two_source_fp4 reads: the "DeepSeek-V4.1 > 40 layers" page,
+ * `_compress_kv`, `fp4_act_quant(latent, 16, True,
+ * scale_dtype=torch.float8_e4m3fn)` (its body is not on the pages; this is the
+ * library's reading).  Per group of 16 features: scale = E4M3(amax / 6), amax
+ * the group's largest magnitude, 6 the largest e2m1 value, the division in
+ * fp32, rounded to the nearest E4M3 value (ties to even, saturating at 448);
+ * each feature's code = e2m1(x / scale) (fp32 division), the nearest of
+ * 0, .5, 1, 1.5, 2, 3, 4, 6 (ties to the even code, saturating at 6), sign in
+ * bit 3 (kept for results of zero); a scale of zero gives codes of zero with
+ * x's sign.  The decoded value code * scale is what the cache then holds.
+ *
+ *   latent      bf16 [rows, D] in device memory, row i at latent + i*row_stride
+ *               elements; 16-byte aligned, row_stride a multiple of 8 and >= D;
+ *               finite or infinite values (a NaN's codes are unspecified)
+ *   D           features per row, a positive multiple of 16
+ *   codes       uint8 [rows, D/2] contiguous, 8-byte aligned: byte j holds
+ *               features 2j (low nibble) and 2j+1 (high nibble)
+ *   scales      uint8 [rows, D/16] contiguous: the E4M3 scale of features
+ *               16g .. 16g+15
+ *
+ * Device memory; asynchronous on `stream`.  SA_ERR_INVALID_ARG for bad sizes,
+ * null or misaligned pointers (before anything is enqueued).  rows == 0 is a
+ * no-op.
+ */
+sa_status sa_fp4_quantize(const void *latent, int64_t rows, int64_t row_stride, int D,
+                          uint8_t *codes, uint8_t *scales, void *stream);
+
+/*
  * Host helper: fill cos_sin_host fp32 [T, rope_dim/2, 2] with
  * (cos, sin)((start_pos + t) * theta ** (-2i / rope_dim)), computed in double.
  * This is the precomputed rotary table of Attention.__init__ (plain theta, no

@@ -20,7 +20,7 @@ from ._build import LIB as _LIB_PATH, LIB_CHECKED as _LIB_CHECKED_PATH, build  #
 
 __all__ = ["sparse_attn", "sparse_attn_two_source", "sparse_attn_two_source_fp4", "sparse_attn_rope_wo_a",
            "sparse_attn_block_tail",
-           "topk_indices", "rope_table", "workspace_size",
+           "topk_indices", "fp4_quantize", "rope_table", "workspace_size",
            "fused_workspace_size", "fused_fp8_workspace_size", "check_errors", "SAError", "library", "build"]
 
 HEADS, HEAD_DIM, MAX_K = 64, 512, 1024
@@ -31,7 +31,7 @@ EXPORTS = ("sa_sparse_attn_workspace_size", "sa_sparse_attn", "sa_sparse_attn_tw
            "sa_rope_table", "sa_check_errors", "sa_status_string", "sa_sparse_attn_noalloc",
            "sa_sparse_attn_block_tail_workspace_size", "sa_sparse_attn_block_tail",
            "sa_topk_indices", "sa_sparse_attn_two_source_fp4", "sa_sparse_attn_rope_wo_a_fp8",
-           "sa_sparse_attn_rope_wo_a_fp8_workspace_size")
+           "sa_sparse_attn_rope_wo_a_fp8_workspace_size", "sa_fp4_quantize")
 
 
 class SAError(RuntimeError):
@@ -85,6 +85,8 @@ def library(path: str | None = None, checked: bool = False) -> ctypes.CDLL:
             lib.sa_sparse_attn_two_source_fp4.restype = I
             lib.sa_sparse_attn_two_source_fp4.argtypes = [V, V, I, L, V, V, I, L, V, V, F, I, I, I, I, I,
                                                           V, I, V, Z, V]
+            lib.sa_fp4_quantize.restype = I
+            lib.sa_fp4_quantize.argtypes = [V, ctypes.c_int64, ctypes.c_int64, I, V, V, V]
             lib.sa_topk_indices.restype = I
             lib.sa_topk_indices.argtypes = [V, ctypes.c_int64, ctypes.c_int64, I, I, I, V, V]
             lib.sa_rope_table.restype = I
@@ -483,6 +485,42 @@ def topk_indices(scores: torch.Tensor, k: int, offset: int = 0, out: torch.Tenso
                                      out.data_ptr() if out.numel() else None, _stream_ptr(stream))
     _check(code, "sa_topk_indices")
     return out
+
+
+def fp4_quantize(latent: torch.Tensor, codes: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                 stream=None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Latent rows bf16 [..., D] -> the fp4 compressed-cache form read by
+    :func:`sparse_attn_two_source_fp4`: (codes uint8 [..., D/2], scales uint8
+    [..., D/16]), an E4M3 scale of amax / 6 per 16 features and e2m1 codes of
+    x / scale (``fp4_act_quant(latent, 16, True, scale_dtype=float8_e4m3fn)``).
+
+    Rows may be strided (stride a multiple of 8 elements); D % 16 == 0."""
+    if not isinstance(latent, torch.Tensor) or latent.dtype != torch.bfloat16 or latent.dim() < 1:
+        raise TypeError("latent must be a bf16 tensor [..., D]")
+    if not latent.is_cuda:
+        raise ValueError("latent must live on a CUDA device")
+    if latent.stride(-1) != 1:
+        raise ValueError("latent rows must be contiguous")
+    D = latent.shape[-1]
+    lead = latent.shape[:-1]
+    rows = 1
+    for n in lead:
+        rows *= int(n)
+    flat = latent.reshape(rows, D)
+    if codes is None:
+        codes = torch.empty((*lead, D // 2), dtype=torch.uint8, device=latent.device)
+    if scales is None:
+        scales = torch.empty((*lead, D // 16), dtype=torch.uint8, device=latent.device)
+    if codes.dtype != torch.uint8 or codes.shape != (*lead, D // 2) or not codes.is_contiguous():
+        raise ValueError("codes must be a contiguous uint8 [..., D/2]")
+    if scales.dtype != torch.uint8 or scales.shape != (*lead, D // 16) or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous uint8 [..., D/16]")
+    if rows == 0:
+        return codes, scales
+    code = library().sa_fp4_quantize(flat.data_ptr(), rows, flat.stride(0), D, codes.data_ptr(),
+                                     scales.data_ptr(), _stream_ptr(stream))
+    _check(code, "sa_fp4_quantize")
+    return codes, scales
 
 
 def block_tail_workspace_size(B: int, T: int, K: int, G: int, R: int) -> int:

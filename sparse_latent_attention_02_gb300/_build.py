@@ -23,7 +23,7 @@ LIB_CHECKED = os.path.join(PKG, "libsa_checked.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 # library -> (extra nvcc flags, object directory)
 VARIANTS = {LIB: ([], BUILD_DIR), LIB_CHECKED: (["-DSA_CHECKED"], os.path.join(BUILD_DIR, "checked"))}
-SOURCES = ["sa_attn.cu", "sa_gemm.cu", "sa_topk.cu", "sa_api.cu", "sa_noalloc.cu"]
+SOURCES = ["sa_attn.cu", "sa_gemm.cu", "sa_topk.cu", "sa_quant.cu", "sa_api.cu", "sa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
 

@@ -601,6 +601,23 @@ sa_status sa_topk_indices(const float *scores, int64_t row_stride, int64_t rows,
                : SA_ERR_CUDA;
 }
 
+sa_status sa_fp4_quantize(const void *latent, int64_t rows, int64_t row_stride, int D, uint8_t *codes,
+                          uint8_t *scales, void *stream)
+{
+    if (rows < 0 || D <= 0 || D % 16 != 0 || row_stride < D || row_stride % 8 != 0)
+        return SA_ERR_INVALID_ARG;
+    if (rows > ((int64_t)1 << 31) * 256 / (D / 16) - 1)
+        return SA_ERR_INVALID_ARG;
+    if (rows == 0)
+        return SA_OK;
+    if (!latent || !codes || !scales || !aligned(latent, 16) || !aligned(codes, 8))
+        return SA_ERR_INVALID_ARG;
+    return launch_fp4_quantize(static_cast<const uint16_t *>(latent), row_stride, rows, D, codes, scales,
+                               static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SA_OK
+               : SA_ERR_CUDA;
+}
+
 sa_status sa_rope_table(double theta, int start_pos, int T, int rope_dim, float *cos_sin_host)
 {
     if (T < 0 || rope_dim <= 0 || rope_dim % 2 != 0 || !(theta > 0.0) || start_pos < 0)

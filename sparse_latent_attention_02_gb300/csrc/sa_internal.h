@@ -107,6 +107,10 @@ cudaError_t launch_wo_a(const GemmParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_dequant_fp8(const uint8_t *w8, const float *scales, uint16_t *w16, int rows, int cols,
                                int num_sms, cudaStream_t st);
 
+// fp4 codes and E4M3 group scales of bf16 latent rows (see sa_fp4_quantize).
+cudaError_t launch_fp4_quantize(const uint16_t *latent, int64_t row_stride, int64_t rows, int D, uint8_t *codes,
+                                uint8_t *scales, cudaStream_t st);
+
 // Top-k selection of positions per row of scores (see sa_topk_indices).
 cudaError_t launch_topk(const float *scores, int64_t row_stride, int64_t rows, int L, int k, int offset,
                         int32_t *out, cudaStream_t st);

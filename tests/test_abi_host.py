@@ -329,3 +329,17 @@ def test_workspace_one_byte_short_is_refused(lib):
         tail = lambda wsb: L.sa_sparse_attn_block_tail(16, 16, 16, 16, 0.1, B, T, 64, 512, 8, K, 16, 64, 16,
                                                        8, 1024, 16, 5120, 16, 256, wsb, None)
         assert tail(bneed - 1) == WORKSPACE and tail(bneed) != WORKSPACE
+
+
+def test_fp4_quantize_host_checks(lib):
+    """sa_fp4_quantize refuses bad sizes and misaligned pointers before any
+    CUDA call (pointers are never dereferenced); zero rows is a no-op."""
+    q = lib.sa_fp4_quantize
+    assert q(256, -1, 512, 512, 256, 256, None) == INVALID
+    assert q(256, 4, 512, 500, 256, 256, None) == INVALID      # D not a multiple of 16
+    assert q(256, 4, 500, 512, 256, 256, None) == INVALID      # row stride below D
+    assert q(256, 4, 516, 512, 256, 256, None) == INVALID      # row stride not a multiple of 8
+    assert q(264, 4, 512, 512, 256, 256, None) == INVALID      # latent not 16-byte aligned
+    assert q(256, 4, 512, 512, 260, 256, None) == INVALID      # codes not 8-byte aligned
+    assert q(None, 4, 512, 512, 256, 256, None) == INVALID
+    assert q(None, 0, 512, 512, None, None, None) == OK       # no rows: nothing to do

@@ -681,3 +681,79 @@ def test_random_shapes_against_oracle(seed):
                                                   512 ** -0.5)
     assert bad == 0
     compare(got4.double().cpu().numpy(), ref4, f"random fp4 {seed}")
+
+
+# ---------------------------------------------------------------- fp4 quantizer
+
+def _special_groups(rng):
+    """Groups of 16 features that exercise the rounding rules: all zero, signed
+    zeros, a scale that underflows E4M3, the bf16 extremes and infinities
+    (scale saturates at 448), values exactly halfway between e2m1 magnitudes
+    (amax 6: scale 1), and a scale rounded down (codes saturate at 6)."""
+    g = []
+    g.append(np.zeros(16))
+    g.append(np.array([-0.0, 0.0] * 8))
+    g.append(np.full(16, 1e-30) * rng.choice([-1, 1], 16))
+    g.append(np.array([3.3895e38, -3.3895e38] + [1.0] * 14))
+    g.append(np.array([np.inf, -2.0, 1e30] + [0.5] * 13))
+    g.append(np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5,
+                       -5.0, 0.0]))
+    g.append(np.array([6.25, -6.25, 3.0, 0.2] + [0.1] * 12))
+    return np.concatenate(g)
+
+
+def test_fp4_quantize_matches_oracle():
+    """Codes and scales bit for bit against the oracle on RMS-normalised latent
+    rows (the cache's inputs), rows of wide dynamic range, the special groups,
+    and strided rows (each row cut from a wider one)."""
+    rng = np.random.default_rng(31)
+    rows, D = 3000, 512
+    x = I.rms_rows(torch.from_numpy(rng.standard_normal((rows, D)).astype(np.float32)))
+    x[100:200] *= torch.from_numpy(np.exp2(rng.integers(-60, 60, (100, 1))).astype(np.float32))
+    spec = _special_groups(rng)
+    x[7, :spec.size] = torch.from_numpy(spec.astype(np.float32))
+    wide = torch.zeros(rows, D + 8, dtype=torch.bfloat16)
+    wide[:, :D] = x.to(torch.bfloat16)
+    lat = wide.cuda()[:, :D]                           # row stride D + 8
+    codes, scales = sa.fp4_quantize(lat)
+    torch.cuda.synchronize()
+    bits = wide[:, :D].contiguous().view(torch.int16).numpy().view(np.uint16)
+    rc, rs = oracle.fp4_quantize(bits)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_fp4_quantized_cache_through_the_attention_call():
+    """The producer and the consumer agree: latents quantized by the library
+    and read by the fp4 call give exactly the bf16 call on the cache the oracle
+    decodes from those codes (and its own codes are the oracle's)."""
+    g = torch.Generator().manual_seed(41)
+    B, T, K, W, C, D = 2, 3, 400, 128, 700, 512
+    win = I.rms_rows(torch.randn(B, W, D, generator=g)).to(torch.bfloat16).cuda()
+    lat = I.rms_rows(torch.randn(B, C, D, generator=g)).to(torch.bfloat16).cuda()
+    codes, scales = sa.fp4_quantize(lat)
+    q = torch.randn(B, T, 64, D, generator=g).to(torch.bfloat16).cuda()
+    sink = torch.randn(64, generator=g).cuda()
+    idx = torch.randint(0, W + C, (B, T, K), generator=g, dtype=torch.int32).cuda()
+    got = sa.sparse_attn_two_source_fp4(q, win, codes, scales, sink, idx, 512 ** -0.5, W=W, C=C,
+                                        out_dtype=torch.float32, check=True)
+    rc, rs = oracle.fp4_quantize(lat.cpu().view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(codes.cpu().numpy(), rc) and np.array_equal(scales.cpu().numpy(), rs)
+    dec = torch.from_numpy(oracle.bf16_bits_exact(oracle.dequant_fp4(rc, rs)).view(np.int16)).view(torch.bfloat16)
+    ref = sa.sparse_attn_two_source(q, win, dec.cuda(), sink, idx, 512 ** -0.5, W=W, C=C,
+                                    out_dtype=torch.float32, check=True)
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("D", [16, 48, 1040])
+def test_fp4_quantize_other_widths(D):
+    """Row widths whose group count is not a power of two (and a single group),
+    against the oracle bit for bit."""
+    rng = np.random.default_rng(D)
+    rows = 777
+    x = torch.from_numpy((rng.standard_normal((rows, D)) * np.exp2(rng.integers(-20, 20, (rows, 1))))
+                         .astype(np.float32)).to(torch.bfloat16)
+    codes, scales = sa.fp4_quantize(x.cuda())
+    rc, rs = oracle.fp4_quantize(x.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
