@@ -4,7 +4,7 @@ error word's bounds bit) gives bit for bit the normal build's results and
 reports no failure, on every entry point and schedule: list pieces merged in
 a cluster, whole queries per CTA, two sources, fp4 rows, the fused tails with
 bf16 and fp8 weights (decoded in the GEMM and decoded first), the block tail,
-the workspace-free call and top-k."""
+the workspace-free call, top-k and the fp4 quantization."""
 import ctypes
 
 import pytest
@@ -128,3 +128,6 @@ def test_checked_noalloc_and_topk():
         sc[:, L // 2:] = torch.where(sc[:, L // 2:] > 1.5, float("-inf"), sc[:, L // 2:])
         a, b = both(lambda: sa.topk_indices(sc, k, offset=128))
         assert torch.equal(a, b)
+    lat = I.rms_rows(torch.randn(300, 512, generator=torch.Generator().manual_seed(4))).to(torch.bfloat16).cuda()
+    (ca, sa_), (cb, sb) = both(lambda: sa.fp4_quantize(lat))
+    assert torch.equal(ca, cb) and torch.equal(sa_, sb)

@@ -58,6 +58,18 @@ MUTATIONS = [
     ("bf16 ties rounded away from zero", PY, "r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "r = (u + 0x8000) >> 16"),
     ("fp8 block scales transposed", PY, "s = np.repeat(np.repeat(sc, FP8_BLOCK",
      "s = np.repeat(np.repeat(sc.T if sc.shape[0] == sc.shape[1] else sc, FP8_BLOCK"),
+    # fp4 quantization
+    ("e2m1 halfway values rounded up", PY,
+     "pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(np.asarray(even)[lo], lo, hi)))",
+     "pick = np.where(dlo < dhi, lo, hi)"),
+    ("fp4 scale over 4 instead of 6", PY, "sb = e4m3_encode(amax / np.float32(6.0))",
+     "sb = e4m3_encode(amax / np.float32(4.0))"),
+    ("fp4 codes without their sign", PY, "return (idx | np.where(np.signbit(x), 8, 0)).astype(np.uint8)",
+     "return idx.astype(np.uint8)"),
+    ("fp4 codes packed with the odd feature low", PY, "codes = (c[..., 0::2] | (c[..., 1::2] << 4))",
+     "codes = (c[..., 1::2] | (c[..., 0::2] << 4))"),
+    ("E4M3 values past 448 to NaN instead of 448", PY, "return np.where(a >= g[-1], len(g) - 1, pick)",
+     "return np.where(a > g[-1], 0x7F, np.where(a == g[-1], len(g) - 1, pick))"),
     # top-k selection
     ("top-k ties to the larger position", PY, "pos[np.lexsort((pos, -row[pos]))]", "pos[np.lexsort((-pos, -row[pos]))]"),
     ("top-k may choose -inf", PY, "~(np.isnan(row) | (row == -np.inf))", "~np.isnan(row)"),
