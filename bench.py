@@ -69,7 +69,7 @@ MEASURED_TRAFFIC = {
     "topk": ("cb7ef0343156eb0625f1156c9ccc55d87b93ab8c532c82af6d0f18a3fe19ce5f", 139_372_857),
     "decode_fp4": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 25_186_662),
     "fused_tail_fp8": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 1_831_613_824),
-    "fp4_quant": ("72256a54edd611e08447f2001cfaf57b4d99696cbe021a19194a03831af11d6b", 323_330_304),
+    "fp4_quant": ("9f2f2da73bfacbbf925cdb6048855baab90b28aabf06e44c25fa463666b8b2a5", 323_808_544),
 }
 
 

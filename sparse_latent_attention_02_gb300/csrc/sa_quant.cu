@@ -84,28 +84,38 @@ __global__ void __launch_bounds__(THREADS) fp4_quant_kernel(const uint16_t *__re
     const uint4 *src = reinterpret_cast<const uint4 *>(latent + r * row_stride + 16 * g);
     const uint4 w[2] = {__ldg(src), __ldg(src + 1)};
     const uint32_t u[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
-    // the group's largest magnitude (non-negative floats order as their bit
-    // patterns): the larger half of each pair, then over the pairs
-    uint32_t amax = 0u;
+    // the group's largest magnitude: a packed maximum over the pairs'
+    // magnitudes, then the larger half (non-negative floats order as their bit
+    // patterns)
+    const uint32_t a0 = u[0] & 0x7FFF7FFFu;
+    __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162 *>(&a0);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-        amax = max(amax, max((u[j] & 0x7FFFu) << 16, u[j] & 0x7FFF0000u));
+    for (int j = 1; j < 8; ++j) {
+        const uint32_t aj = u[j] & 0x7FFF7FFFu;
+        m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162 *>(&aj));
+    }
+    const uint32_t mm = *reinterpret_cast<const uint32_t *>(&m2);
+    const uint32_t amax = max(mm << 16, mm & 0xFFFF0000u);
     float s;
     const uint32_t sb = e4m3_byte(__fdiv_rn(__uint_as_float(amax), 6.0f), s);
-    // thresholds t * scale as bf16 (+1 where a value exactly halfway rounds
-    // down); a scale of zero: NaN thresholds, which no compare passes
+    // thresholds t * scale as bf16 in both halves (+1 where a value exactly
+    // halfway rounds down)
     const float tv[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
     __nv_bfloat162 T[7];
 #pragma unroll
     for (int k = 0; k < 7; ++k) {
-        const uint32_t h = s > 0.f ? (__float_as_uint(tv[k] * s) >> 16) + ((k & 1) == 0 ? 1u : 0u) : 0x7FFFu;
-        const uint32_t hh = h | (h << 16);
+        const uint32_t h = (__float_as_uint(tv[k] * s) >> 16) + ((k & 1) == 0 ? 1u : 0u);
+        const uint32_t hh = h * 0x10001u;
         T[k] = *reinterpret_cast<const __nv_bfloat162 *>(&hh);
     }
     uint32_t c[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         c[j >> 2] |= e2m1_pair(u[j], T) << (8 * (j & 3));
+    if (!(s > 0.f)) {   // a scale of zero: codes of zero with the features' signs
+        c[0] &= 0x88888888u;
+        c[1] &= 0x88888888u;
+    }
     *reinterpret_cast<uint2 *>(codes + r * (int64_t)(8 * groups) + 8 * g) = make_uint2(c[0], c[1]);
     scales[r * groups + g] = (uint8_t)sb;
 }
