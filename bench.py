@@ -66,7 +66,7 @@ MEASURED_TRAFFIC = {
     "prefill": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 1_055_305_024),
     "fused_tail": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 1_789_614_368),
     "block_tail": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 2_776_463_264),
-    "topk": ("cb7ef0343156eb0625f1156c9ccc55d87b93ab8c532c82af6d0f18a3fe19ce5f", 139_372_857),
+    "topk": ("2880efe58a9e4df996f9bd0d61bcf6571513ce84b62392e3fb99bc4054c3dce8", 139_115_691),
     "decode_fp4": ("c0695bcb20121647378ec988ff00bb0b07cf9cfc3132e85185b188a1f781abfc", 25_186_662),
     "fused_tail_fp8": ("3b0734421b6a018e03d32c19911824853d9a61784666510c0d992da5241889ec", 1_831_613_824),
     "fp4_quant": ("9f2f2da73bfacbbf925cdb6048855baab90b28aabf06e44c25fa463666b8b2a5", 323_808_544),

@@ -9,31 +9,34 @@
 //   (masked positions), ties to the smaller position; the chosen positions,
 //   in ascending order, plus `offset`; -1 after them when fewer than k exist.
 //
-// One CTA per row.  Scores become order-preserving 32-bit keys; a three-pass
-// radix select (11, 11 and 10 bits, most significant first) finds the k-th
-// largest key: each pass histograms the keys that share the prefix chosen so
-// far into 2048 bins, and one warp scans the bins, largest first (64 a lane,
-// then two a lane within the lane's range that holds the k-th key), to pick
-// the bin that holds it; the search ends early once that bin is taken whole.  The first pass is folded into the
-// pass that computes the keys, which also finds the last selectable
-// position: the later passes stop there.  The ordered pass gives each warp a
-// contiguous range of positions.  When every key above the threshold is taken
-// and none equal to it (the usual case: only ties leave a share of equal
-// keys), each warp collects its chosen positions in order, with one ballot
-// over 32 positions at a time, in its own segment of the histogram's shared
-// memory, and the segments are written out one after another.  Otherwise the
-// warps first count their keys above the threshold and equal to it, and then
-// write, with ballots, every position above it and the first positions equal
-// to it; either way the output is in ascending position order.  Rows of up to CACHE_KEYS
-// scores keep their keys in shared memory; longer rows are read again from
-// global memory (L2) on every pass.
+// One CTA of four warps per row (with 4096-score rows nine are resident per
+// SM; four warps a row measured faster than two, three, six or eight).
+// Scores become order-preserving
+// 32-bit keys; a three-pass radix select (11, 11 and 10 bits, most significant
+// first) finds the k-th largest key: each pass histograms the keys that share
+// the prefix chosen so far into 2048 bins, and one warp scans the bins,
+// largest first (64 a lane, then two a lane within the lane's range that holds
+// the k-th key), to pick the bin that holds it; the search ends early once
+// that bin is taken whole.  The first pass is folded into the pass that
+// computes the keys, which also finds the last selectable position: the later
+// passes stop there.  The ordered pass gives each warp a contiguous range of
+// positions.  When every key above the threshold is taken and none equal to it
+// (the usual case: only ties leave a share of equal keys), each warp collects
+// its chosen positions in order, with one ballot over 32 positions at a time,
+// in its own segment of the histogram's shared memory, and the segments are
+// written out one after another.  Otherwise the warps first count their keys
+// above the threshold and equal to it, and then write, with ballots, every
+// position above it and the first positions equal to it; either way the output
+// is in ascending position order.  Rows of up to CACHE_KEYS scores keep their
+// keys in shared memory; longer rows are read again from global memory (L2) on
+// every pass.
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
 namespace sa {
 namespace topk {
 
-constexpr int THREADS = 256, WARPS = THREADS / 32;
+constexpr int THREADS = 128, WARPS = THREADS / 32;
 constexpr int CACHE_KEYS = 16384;   // 64 KB of keys in shared memory
 constexpr int BATCH = 16;           // scores a thread loads before it uses any of them
 constexpr int BINS = 2048;          // 11-bit digits
@@ -110,11 +113,11 @@ __device__ __forceinline__ bool find_bin(const int *hist, int need, bool all_if_
     return true;
 }
 // positions a warp can stage in its segment of the histogram's memory (16 bits each)
-constexpr int STAGE_PER_WARP = BINS * 2 / WARPS;   // 512
+constexpr int STAGE_PER_WARP = BINS * 2 / WARPS;   // 1024
 
 // CACHED: the row's keys stay in shared memory (L <= CACHE_KEYS)
 template <bool CACHED>
-__global__ void __launch_bounds__(THREADS, CACHED ? 8 : 6) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
+__global__ void __launch_bounds__(THREADS, CACHED ? 9 : 8) topk_kernel(const float *__restrict__ scores, int64_t row_stride,
                                                        int L, int k, int offset, int32_t *__restrict__ out)
 {
     extern __shared__ __align__(16) uint32_t cache[];   // keys of this row when L <= CACHE_KEYS
